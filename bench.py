@@ -1,0 +1,460 @@
+"""Benchmark: SnapKV compression + compressed-cache decode on the Llama-2-7B-shaped layer.
+
+One step = the whole hot path over one layer of synthetic input resident in HBM:
+snapkv_compress (score statistics -> vote -> max-pool + top-k -> gather + window append) of
+B=1, H=32, d=128 bf16, L_prompt=16384, L_obs=32, K_pool=7, budget 1024, followed by one decode
+step on the compressed cache (snapkv_append of a new token's K/V, then snapkv_decode_attend).
+
+The inputs rotate over 4 resident copies (each 256 MiB of K/V, 1 GiB together, > the 129 MB L2),
+so no step finds its keys in L2 from the step before.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (float64 numpy, one head per step on one core) on the same
+workload. Under torchrun every rank runs its own replica (independent sequences: weak scaling, no
+data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "compressed prompt tok·head·layer/s and decode tok/s; HBM GB/s vs ~8 TB/s"
+UNIT = "tok·head·layer/s"
+WORKLOAD_NAME = ("Llama-2-7B-shaped layer: B1 H32 d128 bf16, L_prompt 16384, L_obs 32, K_pool 7, budget 1024 "
+                 "(64 planted keys/head), + 1 decode step (append + attend) on the compressed cache")
+N_COPIES = 4
+STAGES = ["score", "vote", "topk", "gather"]
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------------------
+# Algorithmic bytes (per head, from the method's definition; intermediates excluded)
+# ------------------------------------------------------------------------------------------------
+
+def algorithmic_bytes(wl, ksel):
+    """Bytes each stage must move per (sequence, head); the vote reads K once and Q_obs."""
+    b = 2 if wl.bf16 else 4
+    d, L, lo = wl.head_dim, wl.l_prompt, wl.l_obs
+    R = ksel + lo
+    return {
+        "score+vote": b * d * (L + lo),                 # every key once + the window queries
+        "gather": 2 * 2 * R * d * b,                    # K and V: R rows read, R rows written
+        "topk": 4 * ksel,                               # the kept indices
+        "decode": b * d * (2 * (R + 1) + 4),            # K+V rows read, q read, o written, append written
+        "step": b * d * (lo + L + 4 * R) + 4 * ksel + b * d * (2 * (R + 1) + 4),
+    }
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(kernel_files):
+    """dram bytes per launch recorded in profiles/ for the dominant kernel, if its source is unchanged."""
+    h = hashlib.sha256()
+    for f in kernel_files:
+        with open(os.path.join(ROOT, "kv_cache_compression_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", "score_vote_llama_layer.md")
+    if not os.path.exists(path):
+        return None, digest
+    text = open(path).read()
+    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_bytes = re.search(r"dram_bytes_per_step:\s*([0-9]+)", text)
+    if not (m_hash and m_bytes) or m_hash.group(1) != digest:
+        return None, digest
+    return int(m_bytes.group(1)), digest
+
+
+# ------------------------------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle timing (spawned worker processes, one BLAS thread each)
+# ------------------------------------------------------------------------------------------------
+
+def _oracle_worker(args):
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    layer_heads, = args
+    import synth
+    from oracle import snapkv_oracle as orc
+    wl = synth.WORKLOADS[1]
+    busy, tokens = 0.0, 0
+    for layer, head in layer_heads:
+        hi = synth.host_head(wl, layer, 0, head, threads=1)
+        qn, kn, vn = synth.host_decode_token(wl, layer, 0, head, 0)
+        t0 = time.perf_counter()
+        ref = orc.compress_head(hi.q_obs, hi.k, hi.v, pool_kernel=wl.pool_kernel, budget=wl.budget)
+        kc, vc = orc.append(ref.k_c, ref.v_c, kn, vn)
+        orc.decode_attend(qn, kc, vc)
+        busy += time.perf_counter() - t0
+        tokens += wl.l_prompt
+    return busy, tokens
+
+
+def cpu_baseline(layers=8):
+    import multiprocessing as mp
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except Exception:
+        cores = os.cpu_count() or 1
+    cores = max(1, min(cores, 64))
+    units = [(layer, h) for layer in range(layers) for h in range(32)]
+    shards = [units[i::cores] for i in range(cores)]
+    env_before = {k: os.environ.get(k) for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in env_before:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(cores) as pool:
+            res = pool.map(_oracle_worker, [(s,) for s in shards if s])
+    finally:
+        for k, v in env_before.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    busy = [r[0] for r in res]
+    tokens = sum(r[1] for r in res)
+    return {"value": tokens / max(busy), "unit": UNIT, "cores": len(res), "kind": "oracle",
+            "sample": f"{layers} layers x 32 heads of the Llama-2-7B-shaped layer (compress + append + decode "
+                      f"per head), {len(res)} processes with one BLAS thread each; value = tokens*heads / "
+                      f"slowest process's compute seconds; total CPU compute {sum(busy):.1f} s"}
+
+
+# ------------------------------------------------------------------------------------------------
+# Reference arm: the CPU oracle
+# ------------------------------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    import synth
+    from oracle import snapkv_oracle as orc
+    wl = synth.WORKLOADS[1]
+    cache = {}
+
+    def inputs(i):
+        h = i % wl.heads
+        if h not in cache:
+            cache[h] = (synth.host_head(wl, 0, 0, h, threads=1), synth.host_decode_token(wl, 0, 0, h, 0))
+        return cache[h]
+
+    def step(i):
+        hi, (qn, kn, vn) = inputs(i)
+        ref = orc.compress_head(hi.q_obs, hi.k, hi.v, pool_kernel=wl.pool_kernel, budget=wl.budget)
+        kc, vc = orc.append(ref.k_c, ref.v_c, kn, vn)
+        return orc.decode_attend(qn, kc, vc)
+
+    for i in range(wl.heads):   # generate every head's input before timing
+        inputs(i)
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = wl.l_prompt * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Philox inputs; no dataset or weights)",
+            "config": {"workload": WORKLOAD_NAME, "global_batch": 1, "seq_len": wl.l_prompt,
+                       "sample": "one head (compress + append + decode) per step, cycling over the 32 heads"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "one head per step on one core (one BLAS thread)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------------
+# Our arm
+# ------------------------------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import ctypes
+
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import synth
+    from kv_cache_compression_gb300 import snapkv
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = synth.WORKLOADS[1]
+    B, H, d, L, lo = 1, wl.heads, wl.head_dim, wl.l_prompt, wl.l_obs
+    params = snapkv.make_params(batch=B, heads=H, head_dim=d, l_obs=lo, l_prompt=L, pool_kernel=wl.pool_kernel,
+                                budget=wl.budget, dtype=snapkv.BF16)
+    ksel = snapkv.kept(params)
+    R = ksel + lo
+    cap = R + 1
+    seq = rank   # each rank compresses its own sequence (independent replica)
+
+    copies = [synth.device_inputs(wl, layer, seq, 1, L, dev)[:3] for layer in range(N_COPIES)]
+    qn, kn, vn = synth.device_decode_tokens(wl, 0, 0, seq, 1, dev)
+    k_out = torch.empty((B, H, cap, d), dtype=torch.bfloat16, device=dev)
+    v_out = torch.empty_like(k_out)
+    length = torch.zeros((B,), dtype=torch.int32, device=dev)
+    idx = torch.empty((B, H, ksel), dtype=torch.int32, device=dev)
+    out = torch.empty((B, H, d), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros((1,), dtype=torch.int32, device=dev)
+    ws_c = snapkv.new_workspace(snapkv.compress_workspace_size(params), dev)
+    ws_d = snapkv.new_workspace(snapkv.decode_workspace_size(B, H, d, cap), dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    lib = snapkv.lib()
+    P = ctypes.c_void_p
+    n_ev = 2 * len(STAGES)
+
+    def launch_step(i, events=None):
+        """Enqueue one step: compress (stage events recorded inside the library), append, decode."""
+        q, k, v = copies[i % N_COPIES]
+        ev_arr = (ctypes.c_void_p * n_ev)(*[e.cuda_event for e in events[:n_ev]]) if events else None
+        st = lib.snapkv_compress_profiled(ctypes.byref(params), P(q.data_ptr()), P(k.data_ptr()), P(v.data_ptr()),
+                                          P(k_out.data_ptr()), P(v_out.data_ptr()), cap, P(length.data_ptr()),
+                                          P(idx.data_ptr()), None, P(ws_c.data_ptr()), ws_c.numel(),
+                                          P(status.data_ptr()), sh, ev_arr, n_ev if events else 0)
+        if st != 0:
+            raise RuntimeError(f"snapkv_compress: {snapkv.status_string(st)}")
+        snapkv.append(kn, vn, k_out, v_out, length, dev_status=status, stream=stream)
+        if events:
+            events[n_ev].record(stream)
+        snapkv.decode_attend(qn, k_out, v_out, length, out=out, workspace=ws_d, dev_status=status, stream=stream)
+        if events:
+            events[n_ev + 1].record(stream)
+
+    # One event set per timed step: the four compress stages (recorded inside the library), then decode.
+    step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev + 2)] for _ in range(args.steps)]
+
+    for i in range(args.warmup):
+        launch_step(i)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {snapkv.status_string(int(status.item()))}")
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)   # let the sampler start before the timed region
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    t_start.record(stream)
+    for i in range(args.steps):
+        launch_step(i, step_events[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {snapkv.status_string(int(status.item()))}")
+
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    units_per_step = B * L * H * 1  # one layer
+    value = units_per_step * world / (ms_per_step * 1e-3)
+
+    stage_ms = {s: statistics.mean(step_events[i][2 * j].elapsed_time(step_events[i][2 * j + 1])
+                                   for i in range(args.steps)) for j, s in enumerate(STAGES + ["decode"])}
+    alg = algorithmic_bytes(wl, ksel)
+    heads = B * H
+    peak, peak_kind = read_peaks()
+    stage_gbs = {
+        "score+vote": alg["score+vote"] * heads / ((stage_ms["score"] + stage_ms["vote"]) * 1e-3) / 1e9,
+        "topk": None,
+        "gather": alg["gather"] * heads / (stage_ms["gather"] * 1e-3) / 1e9,
+        "decode": alg["decode"] * heads / (stage_ms["decode"] * 1e-3) / 1e9,
+    }
+    dominant = max(["score+vote", "topk", "gather", "decode"],
+                   key=lambda s: (stage_ms["score"] + stage_ms["vote"]) if s == "score+vote" else stage_ms[s])
+    dom_ms = (stage_ms["score"] + stage_ms["vote"]) if dominant == "score+vote" else stage_ms[dominant]
+    dom_bytes = alg[dominant] * heads if alg.get(dominant) else 0
+    traffic, src_hash = profiled_traffic(["vote_simt.cu", "snapkv_common.cuh"])
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_bytes else None
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": (achieved / peak) if achieved else None, "peak_source": f"{peak_kind} hbm_gbs",
+                "traffic": traffic if dominant == "score+vote" else None,
+                "alg_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
+                "note": "score+vote = the statistics and vote launches together (the vote re-reads K)"}
+
+    # End to end through the public API with host buffers (pinned), copies inside the timed region.
+    e2e_steps = max(1, min(args.steps, 50))
+    host_in = [tuple(t.to("cpu").pin_memory() for t in c) for c in copies[:2]]
+    host_k = torch.empty((B, H, cap, d), dtype=torch.bfloat16).pin_memory()
+    host_v = torch.empty_like(host_k).pin_memory()
+    host_idx = torch.empty((B, H, ksel), dtype=torch.int32).pin_memory()
+    host_o = torch.empty((B, H, d), dtype=torch.bfloat16).pin_memory()
+    dq, dk, dv = (torch.empty_like(t, device=dev) for t in copies[0])
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        hq, hk, hv = host_in[i % 2]
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        snapkv.compress(dq, dk, dv, pool_kernel=wl.pool_kernel, budget=wl.budget, cap=cap, k_out=k_out, v_out=v_out,
+                        len_out=length, idx_out=idx, workspace=ws_c, dev_status=status, stream=stream)
+        snapkv.append(kn, vn, k_out, v_out, length, dev_status=status, stream=stream)
+        snapkv.decode_attend(qn, k_out, v_out, length, out=out, workspace=ws_d, dev_status=status, stream=stream)
+        host_k.copy_(k_out, non_blocking=True)
+        host_v.copy_(v_out, non_blocking=True)
+        host_idx.copy_(idx, non_blocking=True)
+        host_o.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0])
+    d2h = sum(t.numel() * t.element_size() for t in (host_k, host_v, host_idx, host_o))
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Philox inputs with planted keys; no dataset or weights)",
+        "config": {"workload": WORKLOAD_NAME, "global_batch": B * world, "seq_len": L, "l_obs": lo,
+                   "pool_kernel": wl.pool_kernel, "budget": wl.budget, "kept": ksel, "cap": cap,
+                   "parallelism": f"replicas x{world}", "l2": f"inputs rotate over {N_COPIES} resident copies "
+                   f"({N_COPIES * 2 * B * H * L * d * 2 / 2**20:.0f} MiB of K/V > L2)"},
+        "decode_tok_s": B * world / (stage_ms["decode"] * 1e-3),
+        "hbm_gbs_algorithmic_step": alg["step"] * heads / (ms_per_step * 1e-3) / 1e9,
+        "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
+        "stage_alg_gbs": {k: (round(v, 1) if v else None) for k, v in stage_gbs.items()},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": units_per_step * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "path": "pinned host Q/K/V -> device, snapkv.compress + append + decode_attend, "
+                        "K_c/V_c/idx/out -> pinned host"},
+        "gpu_launches": args.steps * 6,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+        "kernel_source_sha256_16": src_hash,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

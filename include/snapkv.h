@@ -1,0 +1,182 @@
+/*
+ * snapkv.h — C ABI of the GB300 (sm_103a) SnapKV library: prefill-time KV-cache compression and
+ * decode attention over the compressed cache.
+ *
+ * Sources (page title, section / equation):
+ *   [SnapKV]  "論文解説: SnapKV — アテンションパターン観測によるKVキャッシュ圧縮" (0h-n0.github.io,
+ *             posts/paper-2404-14469): プロンプトの分割 (L_prompt = L_prefix + L_obs),
+ *             投票メカニズム (C = sum_i W_obs[:, i, :], I = Top_k(C, k), k = floor(p L_prefix)),
+ *             クラスタリングによる文脈保持 (1D max pooling of C before top-k), アルゴリズム (the
+ *             restated Algorithm 1: snap_kv_compress(query, key, value, obs_window, max_cap,
+ *             kernel) -> (K_c, V_c)), 実装のポイント (per-head independent selection).
+ *   [KVcache] "第22章 KV Cache" (waylandz.com, llm-transformer-book-ja/chapter-22-kv-cache),
+ *             section 22.2: K_cache <- [K_cache; k_t], V_cache <- [V_cache; v_t] and
+ *             o_t = softmax(q_t K_cache^T / sqrt(d_h)) V_cache.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA device pointers of the current device; the library never
+ *     allocates, frees or synchronises, and keeps no state between calls. The caller owns every
+ *     buffer, the workspace and the stream.
+ *   - Work is enqueued asynchronously on `stream`. Argument errors are found on the host before
+ *     anything is enqueued and returned; nothing is launched then.
+ *   - Data-dependent errors found on the GPU (a full cache, a length beyond the capacity, a wait
+ *     that gave up) are OR-ed as snapkv_status bits into *dev_status (device int32, optional:
+ *     NULL disables the report), which the caller reads after synchronising the stream.
+ *   - Tensors are dense, row-major, with the head dimension innermost; every device pointer must
+ *     be 16-byte aligned. Q, K and V of one call share one dtype.
+ */
+#ifndef SNAPKV_H
+#define SNAPKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SNAPKV_API __attribute__((visibility("default")))
+#else
+#define SNAPKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (same type); NULL is the legacy default stream. */
+typedef struct CUstream_st* snapkv_stream_t;
+
+/* Status codes; they are bits, so device-side reports can be OR-ed together. */
+typedef enum {
+  SNAPKV_OK = 0,
+  SNAPKV_ERR_INVALID_ARG = 1,   /* NULL pointer, bad size, misaligned pointer, bad enum       */
+  SNAPKV_ERR_UNSUPPORTED = 2,   /* valid but not implemented: head_dim not 64/128, even pool  */
+  SNAPKV_ERR_CAPACITY = 4,      /* cache capacity too small for k + L_obs, or cache full      */
+  SNAPKV_ERR_CUDA = 8,          /* a CUDA launch failed                                       */
+  SNAPKV_ERR_TIMEOUT = 16,      /* a bounded wait inside a kernel gave up (results invalid)   */
+  SNAPKV_ERR_WORKSPACE = 32,    /* workspace NULL or smaller than the *_workspace_size answer */
+  SNAPKV_ERR_INTERNAL = 64      /* a kernel's own consistency check failed (a library bug)    */
+} snapkv_status;
+
+typedef enum { SNAPKV_F32 = 0, SNAPKV_BF16 = 1 } snapkv_dtype;
+
+/* Which logits enter a window row's softmax (the vote always keeps the prefix columns):
+ *   PROMPT_CAUSAL: all prompt columns the window query sees, i.e. column j <= L_prefix + i for
+ *                  window row i (causal inside the window). This is the default reading.
+ *   PREFIX_ONLY:   the prefix columns only, as the restated Algorithm 1 listing of [SnapKV]
+ *                  (アルゴリズム) normalises them. */
+typedef enum { SNAPKV_SCOPE_PROMPT_CAUSAL = 0, SNAPKV_SCOPE_PREFIX_ONLY = 1 } snapkv_softmax_scope;
+
+/* Problem statement of one compression call: one layer, `batch` sequences of one length. */
+typedef struct {
+  int32_t batch;          /* B >= 1                                                           */
+  int32_t heads;          /* H >= 1 (one KV head per query head)                              */
+  int32_t head_dim;       /* d: 64 or 128                                                     */
+  int32_t l_obs;          /* observation window, 1 <= L_obs < L_prompt ([SnapKV] プロンプトの分割) */
+  int64_t l_prompt;       /* L_prompt; L_prefix = L_prompt - L_obs                             */
+  int32_t pool_kernel;    /* K_pool, odd, >= 1 (stride 1, padding K_pool/2, -inf padding)      */
+  int32_t softmax_scope;  /* snapkv_softmax_scope                                              */
+  double ratio_p;         /* p in [0,1]: k = floor(p * L_prefix) in IEEE double (budget <= 0)  */
+  int64_t budget;         /* > 0: k = min(budget, L_prefix) (the listing's max_cap)            */
+  int32_t dtype;          /* snapkv_dtype of Q, K, V and of the outputs                         */
+  int32_t reserved;       /* must be 0                                                          */
+} snapkv_compress_params;
+
+/* Kept prefix slots per head, k (host-side, for sizing). Returns -1 if the params are invalid. */
+SNAPKV_API int64_t snapkv_compress_kept(const snapkv_compress_params* params);
+
+/* Workspace bytes snapkv_compress needs for these params (0 if the params are invalid). */
+SNAPKV_API size_t snapkv_compress_workspace_size(const snapkv_compress_params* params);
+
+/*
+ * snapkv_compress — SnapKV prefill compression of one layer ([SnapKV] 投票メカニズム,
+ * クラスタリングによる文脈保持, アルゴリズム), per (sequence, head) independently:
+ *   s_ij = q_i . k_j / sqrt(d)                  window query i < L_obs, visible prompt column j
+ *   w_ij = exp(s_ij - m_i) / Z_i                 fp32 row softmax (scope as above)
+ *   C_j  = sum_{i < L_obs} w_ij                 j < L_prefix
+ *   P_j  = max C_{j'} over |j' - j| <= K_pool/2 (clipped to the prefix)
+ *   I    = the k positions of largest P, ties to the lower index, ascending
+ *   K_c  = [K[I]; K[L_prefix : L_prompt]],  V_c likewise   (length R = k + L_obs)
+ *
+ * q_obs     device [B, H, L_obs, d]     the window's queries (prompt rows L_prefix..L_prompt-1)
+ * k, v      device [B, H, L_prompt, d]  the layer's prompt keys and values (not modified)
+ * k_out     device [B, H, cap, d]        rows 0..R-1 of every head are written; the rest untouched
+ * v_out     device [B, H, cap, d]
+ * cap       rows per head of k_out / v_out; must be >= R, else SNAPKV_ERR_CAPACITY
+ * len_out   device int32 [B]             set to R for every sequence
+ * idx_out   device int32 [B, H, k]       kept prefix positions, ascending (NULL: not returned)
+ * vote_out  device fp32 [B, H, L_prefix] the vote C (NULL: not returned)
+ * workspace device, >= snapkv_compress_workspace_size(params) bytes, 256-byte aligned; it must be
+ *           zero-filled before its first use and is left zero-filled in its counter region on
+ *           return, so one workspace can serve every later call (one call at a time)
+ * dev_status device int32 (optional)     error bits OR-ed in on the GPU
+ */
+SNAPKV_API snapkv_status snapkv_compress(const snapkv_compress_params* params, const void* q_obs,
+                              const void* k, const void* v, void* k_out, void* v_out, int64_t cap,
+                              int32_t* len_out, int32_t* idx_out, float* vote_out,
+                              void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              snapkv_stream_t stream);
+
+/*
+ * snapkv_compress_profiled — snapkv_compress, plus caller-created CUDA events (cudaEvent_t, cast
+ * to void*) recorded on `stream` around the kernels of each stage, so that a caller can time
+ * every stage on the device: stage_events[2s] is recorded just before and stage_events[2s+1]
+ * just after the kernels of stage s, with s = 0 score statistics (row max and sum of every
+ * window row), 1 vote, 2 max-pool + top-k, 3 gather + window append. Slots beyond n_events, or
+ * NULL entries, are skipped; n_events = 0 behaves exactly like snapkv_compress. The events are
+ * owned by the caller. A stage that needs no kernel for the given problem records its two
+ * events back to back.
+ */
+SNAPKV_API snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, const void* q_obs,
+                                                  const void* k, const void* v, void* k_out, void* v_out,
+                                                  int64_t cap, int32_t* len_out, int32_t* idx_out,
+                                                  float* vote_out, void* workspace, size_t workspace_bytes,
+                                                  int32_t* dev_status, snapkv_stream_t stream,
+                                                  void* const* stage_events, int32_t n_events);
+
+/*
+ * snapkv_append — one decode step's cache append ([KVcache] 22.2): for every sequence b and
+ * head h, row len[b] of k_cache / v_cache receives k_new / v_new, then len[b] += 1.
+ *
+ * k_new, v_new      device [B, H, d]
+ * k_cache, v_cache  device [B, H, cap, d]
+ * len               device int32 [B], current cached rows per sequence (read, then incremented)
+ * A sequence with len[b] >= cap (or < 0) is left untouched and SNAPKV_ERR_CAPACITY is reported in
+ * *dev_status.
+ */
+SNAPKV_API snapkv_status snapkv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                            int64_t cap, int32_t* len, int32_t batch, int32_t heads,
+                            int32_t head_dim, int32_t dtype, int32_t* dev_status,
+                            snapkv_stream_t stream);
+
+/* Workspace bytes snapkv_decode_attend needs (0 if the sizes are invalid). */
+SNAPKV_API size_t snapkv_decode_workspace_size(int32_t batch, int32_t heads, int32_t head_dim, int64_t cap);
+
+/*
+ * snapkv_decode_attend — decode attention over each head's (compressed) cache ([KVcache] 22.2):
+ *   o = softmax(q . K_cache[r]^T / sqrt(d), r < len[b]) V_cache     (fp32 math)
+ * Every cached row is visible (the query is the newest position).
+ *
+ * q                 device [B, H, d]
+ * k_cache, v_cache  device [B, H, cap, d]
+ * len               device int32 [B]; rows 0..len[b]-1 are attended. len[b] > cap is clamped to
+ *                   cap and reported as SNAPKV_ERR_CAPACITY; len[b] <= 0 gives o = 0.
+ * out               device [B, H, d], same dtype as the cache
+ * workspace         device, >= snapkv_decode_workspace_size(...) bytes, 256-byte aligned,
+ *                   zero-filled before first use (its counters are left zeroed on return)
+ */
+SNAPKV_API snapkv_status snapkv_decode_attend(const void* q, const void* k_cache, const void* v_cache,
+                                   int64_t cap, const int32_t* len, void* out, int32_t batch,
+                                   int32_t heads, int32_t head_dim, int32_t dtype, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_status,
+                                   snapkv_stream_t stream);
+
+/* Human-readable name of a status value (a static string; bits are listed when several). */
+SNAPKV_API const char* snapkv_status_string(int32_t status);
+
+/* ABI version of this header (major * 100 + minor). */
+SNAPKV_API int32_t snapkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SNAPKV_H */

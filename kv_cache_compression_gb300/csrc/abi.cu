@@ -1,0 +1,247 @@
+// C ABI of the SnapKV library: argument validation, workspace layout and launch order.
+// Every argument error is found here, on the host, before anything is enqueued.
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "snapkv_common.cuh"
+#include "snapkv_internal.h"
+
+namespace snapkv {
+
+namespace {
+
+constexpr int kVoteChunk = 1024;   // prompt columns per CTA of the score/vote kernels
+constexpr int64_t kMaxPrompt = (int64_t)1 << 30;
+constexpr int kMaxObs = 128;
+
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+// Validates the problem statement; on success fills l_prefix and k_sel.
+snapkv_status check_params(const snapkv_compress_params* p, int64_t* l_prefix, int64_t* k_sel) {
+  if (!p) return SNAPKV_ERR_INVALID_ARG;
+  if (p->batch < 1 || p->heads < 1 || p->head_dim < 1 || p->l_obs < 1 || p->pool_kernel < 1)
+    return SNAPKV_ERR_INVALID_ARG;
+  if (p->l_prompt <= p->l_obs || p->l_prompt > kMaxPrompt) return SNAPKV_ERR_INVALID_ARG;
+  if (p->softmax_scope != SNAPKV_SCOPE_PROMPT_CAUSAL && p->softmax_scope != SNAPKV_SCOPE_PREFIX_ONLY)
+    return SNAPKV_ERR_INVALID_ARG;
+  if (p->dtype != SNAPKV_F32 && p->dtype != SNAPKV_BF16) return SNAPKV_ERR_INVALID_ARG;
+  if (p->reserved != 0) return SNAPKV_ERR_INVALID_ARG;
+  if (p->budget <= 0 && !(p->ratio_p >= 0.0 && p->ratio_p <= 1.0)) return SNAPKV_ERR_INVALID_ARG;
+  if ((int64_t)p->batch * p->heads > 65535) return SNAPKV_ERR_INVALID_ARG;  // grid.y limit
+  if (p->head_dim != 64 && p->head_dim != 128) return SNAPKV_ERR_UNSUPPORTED;
+  if (p->pool_kernel % 2 == 0) return SNAPKV_ERR_UNSUPPORTED;
+  if (p->l_obs > kMaxObs) return SNAPKV_ERR_UNSUPPORTED;
+  const int64_t lp = p->l_prompt - p->l_obs;
+  int64_t k;
+  if (p->budget > 0)
+    k = p->budget < lp ? p->budget : lp;
+  else
+    k = (int64_t)floor(p->ratio_p * (double)lp);
+  if (k < 0) k = 0;
+  if (k > lp) k = lp;
+  *l_prefix = lp;
+  *k_sel = k;
+  return SNAPKV_OK;
+}
+
+}  // namespace
+
+CompressLayout compress_layout(int batch, int heads, int l_obs, int64_t l_prompt, int64_t k_sel) {
+  CompressLayout L;
+  const size_t bh = (size_t)batch * heads;
+  const int64_t l_prefix = l_prompt - l_obs;
+  L.vote_chunk = kVoteChunk;
+  L.n_chunk_all = (int)((l_prompt + kVoteChunk - 1) / kVoteChunk);
+  L.n_chunk_prefix = (int)((l_prefix + kVoteChunk - 1) / kVoteChunk);
+  L.partial = 0;
+  L.c = up256(bh * L.n_chunk_all * l_obs * 2 * sizeof(float));
+  L.p = L.c + up256(bh * l_prefix * sizeof(float));
+  L.idx = L.p + up256(bh * l_prefix * sizeof(float));
+  L.total = L.idx + up256(bh * (k_sel > 0 ? k_sel : 1) * sizeof(int32_t));
+  return L;
+}
+
+}  // namespace snapkv
+
+using namespace snapkv;
+
+extern "C" {
+
+int32_t snapkv_abi_version(void) { return 100; }
+
+const char* snapkv_status_string(int32_t status) {
+  switch (status) {
+    case SNAPKV_OK: return "SNAPKV_OK";
+    case SNAPKV_ERR_INVALID_ARG: return "SNAPKV_ERR_INVALID_ARG";
+    case SNAPKV_ERR_UNSUPPORTED: return "SNAPKV_ERR_UNSUPPORTED";
+    case SNAPKV_ERR_CAPACITY: return "SNAPKV_ERR_CAPACITY";
+    case SNAPKV_ERR_CUDA: return "SNAPKV_ERR_CUDA";
+    case SNAPKV_ERR_TIMEOUT: return "SNAPKV_ERR_TIMEOUT";
+    case SNAPKV_ERR_WORKSPACE: return "SNAPKV_ERR_WORKSPACE";
+    case SNAPKV_ERR_INTERNAL: return "SNAPKV_ERR_INTERNAL";
+    default: break;
+  }
+  if (status < 0 || status > 127) return "SNAPKV_ERR_UNKNOWN";
+  // Several bits: a fixed table of combinations is not worth it; name the highest-priority one.
+  if (status & SNAPKV_ERR_INTERNAL) return "SNAPKV_ERR_INTERNAL|...";
+  if (status & SNAPKV_ERR_TIMEOUT) return "SNAPKV_ERR_TIMEOUT|...";
+  if (status & SNAPKV_ERR_CUDA) return "SNAPKV_ERR_CUDA|...";
+  if (status & SNAPKV_ERR_CAPACITY) return "SNAPKV_ERR_CAPACITY|...";
+  if (status & SNAPKV_ERR_WORKSPACE) return "SNAPKV_ERR_WORKSPACE|...";
+  if (status & SNAPKV_ERR_UNSUPPORTED) return "SNAPKV_ERR_UNSUPPORTED|...";
+  return "SNAPKV_ERR_INVALID_ARG|...";
+}
+
+int64_t snapkv_compress_kept(const snapkv_compress_params* params) {
+  int64_t lp = 0, k = 0;
+  if (check_params(params, &lp, &k) != SNAPKV_OK) return -1;
+  return k;
+}
+
+size_t snapkv_compress_workspace_size(const snapkv_compress_params* params) {
+  int64_t lp = 0, k = 0;
+  if (check_params(params, &lp, &k) != SNAPKV_OK) return 0;
+  return compress_layout(params->batch, params->heads, params->l_obs, params->l_prompt, k).total;
+}
+
+snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, const void* q_obs, const void* k,
+                                       const void* v, void* k_out, void* v_out, int64_t cap, int32_t* len_out,
+                                       int32_t* idx_out, float* vote_out, void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_status, snapkv_stream_t stream, void* const* stage_events,
+                                       int32_t n_events) {
+  if (n_events < 0 || (n_events > 0 && !stage_events)) return SNAPKV_ERR_INVALID_ARG;
+  int64_t l_prefix = 0, k_sel = 0;
+  const snapkv_status st = check_params(params, &l_prefix, &k_sel);
+  if (st != SNAPKV_OK) return st;
+  if (!q_obs || !k || !v || !k_out || !v_out || !len_out) return SNAPKV_ERR_INVALID_ARG;
+  if (!aligned16(q_obs) || !aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out))
+    return SNAPKV_ERR_INVALID_ARG;
+  if (((uintptr_t)len_out & 3u) || ((uintptr_t)idx_out & 3u) || ((uintptr_t)vote_out & 3u) ||
+      ((uintptr_t)dev_status & 3u))
+    return SNAPKV_ERR_INVALID_ARG;
+  if (cap < k_sel + params->l_obs || cap > kMaxPrompt) return SNAPKV_ERR_CAPACITY;
+  const CompressLayout L = compress_layout(params->batch, params->heads, params->l_obs, params->l_prompt, k_sel);
+  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SNAPKV_ERR_WORKSPACE;
+
+  const size_t esize = params->dtype == SNAPKV_BF16 ? 2 : 4;
+  const size_t bh = (size_t)params->batch * params->heads;
+  const size_t in_bytes = bh * (size_t)params->l_prompt * params->head_dim * esize;
+  const size_t out_bytes = bh * (size_t)cap * params->head_dim * esize;
+  if (overlaps(k, in_bytes, k_out, out_bytes) || overlaps(k, in_bytes, v_out, out_bytes) ||
+      overlaps(v, in_bytes, k_out, out_bytes) || overlaps(v, in_bytes, v_out, out_bytes) ||
+      overlaps(k_out, out_bytes, v_out, out_bytes))
+    return SNAPKV_ERR_INVALID_ARG;
+
+  char* ws = static_cast<char*>(workspace);
+  CompressJob job;
+  job.batch = params->batch;
+  job.heads = params->heads;
+  job.head_dim = params->head_dim;
+  job.l_obs = params->l_obs;
+  job.pool_kernel = params->pool_kernel;
+  job.scope = params->softmax_scope;
+  job.dtype = params->dtype;
+  job.l_prompt = params->l_prompt;
+  job.l_prefix = l_prefix;
+  job.k_sel = k_sel;
+  job.cap = cap;
+  job.q_obs = q_obs;
+  job.k = k;
+  job.v = v;
+  job.k_out = k_out;
+  job.v_out = v_out;
+  job.len_out = len_out;
+  job.idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
+  job.c = vote_out ? vote_out : reinterpret_cast<float*>(ws + L.c);
+  job.p = reinterpret_cast<float*>(ws + L.p);
+  job.partial = reinterpret_cast<float*>(ws + L.partial);
+  job.vote_chunk = L.vote_chunk;
+  job.n_chunk_all = L.n_chunk_all;
+  job.n_chunk_prefix = L.n_chunk_prefix;
+  job.dev_status = dev_status;
+  job.stream = reinterpret_cast<cudaStream_t>(stream);
+  job.events = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(stage_events));
+  job.n_events = n_events;
+
+  if (launch_vote_simt(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  if (launch_pool_topk(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  if (launch_gather(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  return SNAPKV_OK;
+}
+
+snapkv_status snapkv_compress(const snapkv_compress_params* params, const void* q_obs, const void* k,
+                              const void* v, void* k_out, void* v_out, int64_t cap, int32_t* len_out,
+                              int32_t* idx_out, float* vote_out, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_status, snapkv_stream_t stream) {
+  return snapkv_compress_profiled(params, q_obs, k, v, k_out, v_out, cap, len_out, idx_out, vote_out, workspace,
+                                  workspace_bytes, dev_status, stream, nullptr, 0);
+}
+
+snapkv_status snapkv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int64_t cap,
+                            int32_t* len, int32_t batch, int32_t heads, int32_t head_dim, int32_t dtype,
+                            int32_t* dev_status, snapkv_stream_t stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !len) return SNAPKV_ERR_INVALID_ARG;
+  if (batch < 1 || heads < 1 || head_dim < 1 || cap < 1 || cap > kMaxPrompt) return SNAPKV_ERR_INVALID_ARG;
+  if (dtype != SNAPKV_F32 && dtype != SNAPKV_BF16) return SNAPKV_ERR_INVALID_ARG;
+  if ((int64_t)batch * heads > 65535) return SNAPKV_ERR_INVALID_ARG;  // grid.y limit
+  if (head_dim != 64 && head_dim != 128) return SNAPKV_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      ((uintptr_t)len & 3u) || ((uintptr_t)dev_status & 3u))
+    return SNAPKV_ERR_INVALID_ARG;
+  if (launch_append(k_new, v_new, k_cache, v_cache, cap, len, batch, heads, head_dim, dtype, dev_status,
+                    reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SNAPKV_ERR_CUDA;
+  return SNAPKV_OK;
+}
+
+size_t snapkv_decode_workspace_size(int32_t batch, int32_t heads, int32_t head_dim, int64_t cap) {
+  if (batch < 1 || heads < 1 || cap < 1 || cap > kMaxPrompt) return 0;
+  if (head_dim != 64 && head_dim != 128) return 0;
+  return decode_layout(batch, heads, head_dim, cap).total;
+}
+
+snapkv_status snapkv_decode_attend(const void* q, const void* k_cache, const void* v_cache, int64_t cap,
+                                   const int32_t* len, void* out, int32_t batch, int32_t heads, int32_t head_dim,
+                                   int32_t dtype, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                   snapkv_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !len || !out) return SNAPKV_ERR_INVALID_ARG;
+  if (batch < 1 || heads < 1 || head_dim < 1 || cap < 1 || cap > kMaxPrompt) return SNAPKV_ERR_INVALID_ARG;
+  if (dtype != SNAPKV_F32 && dtype != SNAPKV_BF16) return SNAPKV_ERR_INVALID_ARG;
+  if ((int64_t)batch * heads > 65535) return SNAPKV_ERR_INVALID_ARG;  // grid.y limit
+  if (head_dim != 64 && head_dim != 128) return SNAPKV_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || ((uintptr_t)len & 3u) ||
+      ((uintptr_t)dev_status & 3u))
+    return SNAPKV_ERR_INVALID_ARG;
+  const DecodeLayout L = decode_layout(batch, heads, head_dim, cap);
+  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SNAPKV_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  DecodeJob job;
+  job.batch = batch;
+  job.heads = heads;
+  job.head_dim = head_dim;
+  job.dtype = dtype;
+  job.cap = cap;
+  job.q = q;
+  job.k_cache = k_cache;
+  job.v_cache = v_cache;
+  job.len = len;
+  job.out = out;
+  job.partial = reinterpret_cast<float*>(ws + L.partial);
+  job.tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
+  job.split_rows = L.split_rows;
+  job.n_split = L.n_split;
+  job.dev_status = dev_status;
+  job.stream = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_decode(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  return SNAPKV_OK;
+}
+
+}  // extern "C"

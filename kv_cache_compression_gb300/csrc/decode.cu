@@ -1,0 +1,259 @@
+// Decode-step append and split-K decode attention over the (compressed) cache.
+//
+// KV-cache chapter ("第22章 KV Cache"), section 22.2: K_cache <- [K_cache; k_t],
+// V_cache <- [V_cache; v_t], then o_t = softmax(q_t K_cache^T / sqrt(d_h)) V_cache with every cached
+// row visible. Each (sequence, head) cache is cut into splits of `split_rows` rows; one CTA per
+// split keeps an online softmax (running max m, running sum l, unnormalised output o) in the log2
+// domain, writes (m, l, o) to the workspace, and the last CTA of the head to finish (an atomic
+// ticket, no waiting) merges the splits and writes o / l.
+#include "snapkv_common.cuh"
+#include "snapkv_internal.h"
+
+namespace snapkv {
+namespace {
+
+constexpr int kDecThreads = 128;
+constexpr int kSplitRows = 256;
+
+__global__ void __launch_bounds__(256)
+append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, uint4* __restrict__ k_cache,
+              uint4* __restrict__ v_cache, int64_t cap, int32_t* __restrict__ len, int heads, int vpr,
+              int32_t* __restrict__ dev_status) {
+  __shared__ int pos;
+  const int b = blockIdx.x;
+  if (threadIdx.x == 0) {
+    const int p = len[b];
+    pos = (p >= 0 && (int64_t)p < cap) ? p : -1;
+    if (pos < 0) report(dev_status, SNAPKV_ERR_CAPACITY);
+  }
+  __syncthreads();
+  if (pos < 0) return;
+  for (int u = threadIdx.x; u < heads * vpr; u += blockDim.x) {
+    const int h = u / vpr, c = u % vpr;
+    const int64_t bh = (int64_t)b * heads + h;
+    k_cache[(bh * cap + pos) * vpr + c] = k_new[bh * vpr + c];
+    v_cache[(bh * cap + pos) * vpr + c] = v_new[bh * vpr + c];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) len[b] = pos + 1;
+}
+
+struct DecArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* len;
+  void* out;
+  float* partial;
+  uint32_t* tickets;
+  int64_t cap;
+  int heads, split_rows, n_split;
+  float scale_log2;
+  int32_t* dev_status;
+};
+
+template <typename T> __device__ __forceinline__ void store_out(T* p, float x);
+template <> __device__ __forceinline__ void store_out<float>(float* p, float x) { *p = x; }
+template <> __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* p, float x) {
+  *p = __float2bfloat16_rn(x);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecArgs a) {
+  constexpr int V = Elem<T>::kVec;
+  constexpr int LPR = D / V;                       // lanes per cache row
+  constexpr int RPW = 32 / LPR;                    // rows per warp step
+  constexpr int GROUPS = (kDecThreads / 32) * RPW; // row groups per CTA
+  constexpr int UNROLL = 4;
+  __shared__ float sm_m[GROUPS], sm_l[GROUPS];
+  __shared__ __align__(16) float sm_o[GROUPS][D];
+  __shared__ int sh_last;
+
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  const int split = blockIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int b = (int)(bh / a.heads);
+  int n = a.len[b];
+  if ((int64_t)n > a.cap) {
+    if (split == 0 && tid == 0 && bh % a.heads == 0) report(a.dev_status, SNAPKV_ERR_CAPACITY);
+    n = (int)a.cap;
+  }
+  if (n < 0) n = 0;
+  const int r0 = split * a.split_rows;
+  const int r1 = min(n, r0 + a.split_rows);
+  const int sub = lane / LPR, cl = lane % LPR;
+  const int group = warp * RPW + sub;
+
+  const T* qp = static_cast<const T*>(a.q) + bh * D;
+  float q[V];
+  Elem<T>::widen(ld_nc_v4(qp + cl * V), q);
+#pragma unroll
+  for (int e = 0; e < V; ++e) q[e] *= a.scale_log2;
+
+  const T* kc = static_cast<const T*>(a.k_cache) + bh * a.cap * D + cl * V;
+  const T* vc = static_cast<const T*>(a.v_cache) + bh * a.cap * D + cl * V;
+  float m = -INFINITY, l = 0.f, o[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) o[e] = 0.f;
+
+  // The trip count depends only on the split, so every lane of a warp runs the same iterations
+  // (the row reductions below shuffle across the whole warp).
+  for (int base = r0; base < r1; base += GROUPS * UNROLL) {
+    const int rb = base + group;
+    uint4 kr[UNROLL], vr[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int r = rb + u * GROUPS;
+      if (r < r1) {
+        kr[u] = ld_stream_v4(kc + (int64_t)r * D);
+        vr[u] = ld_stream_v4(vc + (int64_t)r * D);
+      } else {
+        kr[u] = make_uint4(0, 0, 0, 0);
+        vr[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    float s[UNROLL];
+    float smax = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      float kf[V];
+      Elem<T>::widen(kr[u], kf);
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < V; ++e) dot = fmaf(q[e], kf[e], dot);
+#pragma unroll
+      for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      s[u] = (rb + u * GROUPS < r1) ? dot : -INFINITY;
+      smax = fmaxf(smax, s[u]);
+    }
+    const float m_new = fmaxf(m, smax);
+    if (m_new == -INFINITY) continue;
+    const float corr = ex2(m - m_new);
+    l *= corr;
+#pragma unroll
+    for (int e = 0; e < V; ++e) o[e] *= corr;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const float p = ex2(s[u] - m_new);
+      float vf[V];
+      Elem<T>::widen(vr[u], vf);
+      l += p;
+#pragma unroll
+      for (int e = 0; e < V; ++e) o[e] = fmaf(p, vf[e], o[e]);
+    }
+    m = m_new;
+  }
+
+  if (cl == 0) {
+    sm_m[group] = m;
+    sm_l[group] = l;
+  }
+#pragma unroll
+  for (int e = 0; e < V; ++e) sm_o[group][cl * V + e] = o[e];
+  __syncthreads();
+
+  float* part = a.partial + (bh * a.n_split + split) * (D + 2);
+  for (int t = tid; t < D; t += kDecThreads) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < GROUPS; ++g) M = fmaxf(M, sm_m[g]);
+    float ot = 0.f, lt = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int g = 0; g < GROUPS; ++g) {
+        if (sm_m[g] == -INFINITY) continue;
+        const float w = ex2(sm_m[g] - M);
+        ot = fmaf(sm_o[g][t], w, ot);
+        lt = fmaf(sm_l[g], w, lt);
+      }
+    }
+    part[t] = ot;
+    if (t == 0) {
+      part[D] = M;
+      part[D + 1] = lt;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t ticket = atomicAdd(a.tickets + bh, 1u);
+    sh_last = ticket == (uint32_t)(a.n_split - 1);
+  }
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  const float* parts = a.partial + bh * a.n_split * (D + 2);
+  T* out = static_cast<T*>(a.out) + bh * D;
+  for (int t = tid; t < D; t += kDecThreads) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < a.n_split; ++sp) M = fmaxf(M, __ldcg(parts + sp * (D + 2) + D));
+    float ot = 0.f, lt = 0.f;
+    if (M != -INFINITY) {
+      for (int sp = 0; sp < a.n_split; ++sp) {
+        const float ms = __ldcg(parts + sp * (D + 2) + D);
+        if (ms == -INFINITY) continue;
+        const float w = ex2(ms - M);
+        ot = fmaf(__ldcg(parts + sp * (D + 2) + t), w, ot);
+        lt = fmaf(__ldcg(parts + sp * (D + 2) + D + 1), w, lt);
+      }
+    }
+    store_out<T>(out + t, lt > 0.f ? ot / lt : 0.f);
+  }
+  if (tid == 0) a.tickets[bh] = 0u;
+}
+
+template <typename T, int D>
+cudaError_t launch_decode_typed(const DecodeJob& job, const DecArgs& a) {
+  const int64_t bh = (int64_t)job.batch * job.heads;
+  decode_split_kernel<T, D><<<dim3(job.n_split, (unsigned)bh), kDecThreads, 0, job.stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+DecodeLayout decode_layout(int batch, int heads, int head_dim, int64_t cap) {
+  DecodeLayout L;
+  L.split_rows = kSplitRows;
+  L.n_split = (int)((cap + kSplitRows - 1) / kSplitRows);
+  if (L.n_split < 1) L.n_split = 1;
+  const size_t bh = (size_t)batch * heads;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  L.partial = 0;
+  L.tickets = up(bh * L.n_split * (head_dim + 2) * sizeof(float));
+  L.total = up(L.tickets + bh * sizeof(uint32_t));
+  return L;
+}
+
+cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int64_t cap,
+                          int32_t* len, int batch, int heads, int head_dim, int dtype, int32_t* dev_status,
+                          cudaStream_t stream) {
+  const int esize = dtype == SNAPKV_BF16 ? 2 : 4;
+  const int vpr = head_dim * esize / 16;
+  append_kernel<<<batch, 256, 0, stream>>>(static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                                           static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), cap, len,
+                                           heads, vpr, dev_status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeJob& job) {
+  DecArgs a;
+  a.q = job.q;
+  a.k_cache = job.k_cache;
+  a.v_cache = job.v_cache;
+  a.len = job.len;
+  a.out = job.out;
+  a.partial = job.partial;
+  a.tickets = job.tickets;
+  a.cap = job.cap;
+  a.heads = job.heads;
+  a.split_rows = job.split_rows;
+  a.n_split = job.n_split;
+  a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)job.head_dim));
+  a.dev_status = job.dev_status;
+  if (job.dtype == SNAPKV_BF16)
+    return job.head_dim == 64 ? launch_decode_typed<__nv_bfloat16, 64>(job, a)
+                              : launch_decode_typed<__nv_bfloat16, 128>(job, a);
+  return job.head_dim == 64 ? launch_decode_typed<float, 64>(job, a) : launch_decode_typed<float, 128>(job, a);
+}
+
+}  // namespace snapkv

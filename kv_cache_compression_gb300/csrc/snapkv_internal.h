@@ -1,0 +1,78 @@
+// Internal launcher interface between the C ABI layer (abi.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace snapkv {
+
+// One compression call, after host-side validation.
+struct CompressJob {
+  int batch, heads, head_dim, l_obs, pool_kernel, scope, dtype;
+  int64_t l_prompt, l_prefix, k_sel, cap;
+  const void* q_obs;
+  const void* k;
+  const void* v;
+  void* k_out;
+  void* v_out;
+  int32_t* len_out;
+  int32_t* idx;        // kept indices (caller's buffer or workspace)
+  float* c;            // vote (caller's buffer or workspace)
+  float* p;            // pooled vote (workspace)
+  float* partial;      // per-chunk row statistics (workspace)
+  int vote_chunk;      // keys per chunk of the score/vote kernels
+  int n_chunk_all;     // chunks covering the whole prompt
+  int n_chunk_prefix;  // chunks covering the prefix
+  int32_t* dev_status;
+  cudaStream_t stream;
+  cudaEvent_t* events;  // optional stage events (see snapkv_compress_profiled), may be null
+  int n_events;
+  void mark(int slot) const {
+    if (events && slot < n_events && events[slot]) cudaEventRecord(events[slot], stream);
+  }
+};
+
+// Stage event slots: events[2s] before and events[2s+1] after the kernels of stage s.
+enum { kStageScore = 0, kStageVote = 1, kStageTopk = 2, kStageGather = 3, kStages = 4 };
+
+// Workspace layout of a compression call (byte offsets, each 256-aligned).
+struct CompressLayout {
+  size_t partial, c, p, idx, total;
+  int vote_chunk, n_chunk_all, n_chunk_prefix;
+};
+
+CompressLayout compress_layout(int batch, int heads, int l_obs, int64_t l_prompt, int64_t k_sel);
+
+cudaError_t launch_vote_simt(const CompressJob& job);
+cudaError_t launch_pool_topk(const CompressJob& job);
+cudaError_t launch_gather(const CompressJob& job);
+
+struct DecodeJob {
+  int batch, heads, head_dim, dtype;
+  int64_t cap;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* len;
+  void* out;
+  float* partial;       // [B*H][n_split][d + 2]
+  uint32_t* tickets;    // [B*H]
+  int split_rows, n_split;
+  int32_t* dev_status;
+  cudaStream_t stream;
+};
+
+struct DecodeLayout {
+  size_t partial, tickets, total;
+  int split_rows, n_split;
+};
+
+DecodeLayout decode_layout(int batch, int heads, int head_dim, int64_t cap);
+
+cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                          int64_t cap, int32_t* len, int batch, int heads, int head_dim, int dtype,
+                          int32_t* dev_status, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeJob& job);
+
+}  // namespace snapkv

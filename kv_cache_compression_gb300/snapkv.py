@@ -1,0 +1,204 @@
+"""Python binding of libsnapkv.so (ctypes). Argument marshalling only.
+
+Every computation runs in the library's CUDA kernels; this module only turns torch tensors into
+device pointers and a stream handle, allocates outputs and workspaces with torch when the caller
+does not pass them, and raises on a non-OK status. There is no CPU or PyTorch fallback: if the
+library is missing the import of the first call fails.
+
+The functions and their arguments mirror include/snapkv.h (see that header for the layouts and
+the passages of the pages each operation follows).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libsnapkv.so")
+_HEADER = os.path.join(os.path.dirname(_HERE), "include", "snapkv.h")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_INTERNAL = (
+    0, 1, 2, 4, 8, 16, 32, 64)
+F32, BF16 = 0, 1
+SCOPE_PROMPT_CAUSAL, SCOPE_PREFIX_ONLY = 0, 1
+_SCOPES = {"prompt_causal": SCOPE_PROMPT_CAUSAL, "prefix_only": SCOPE_PREFIX_ONLY}
+
+
+class CompressParams(ctypes.Structure):
+    """Mirror of snapkv_compress_params."""
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("l_obs", ctypes.c_int32), ("l_prompt", ctypes.c_int64), ("pool_kernel", ctypes.c_int32),
+        ("softmax_scope", ctypes.c_int32), ("ratio_p", ctypes.c_double), ("budget", ctypes.c_int64),
+        ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    ]
+
+
+class SnapKVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libsnapkv.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(there is no fallback path)")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        PP = ctypes.POINTER(CompressParams)
+        L.snapkv_compress_kept.restype = I64
+        L.snapkv_compress_kept.argtypes = [PP]
+        L.snapkv_compress_workspace_size.restype = SZ
+        L.snapkv_compress_workspace_size.argtypes = [PP]
+        L.snapkv_compress.restype = I32
+        L.snapkv_compress.argtypes = [PP, P, P, P, P, P, I64, P, P, P, P, SZ, P, P]
+        L.snapkv_append.restype = I32
+        L.snapkv_append.argtypes = [P, P, P, P, I64, P, I32, I32, I32, I32, P, P]
+        L.snapkv_decode_workspace_size.restype = SZ
+        L.snapkv_decode_workspace_size.argtypes = [I32, I32, I32, I64]
+        L.snapkv_decode_attend.restype = I32
+        L.snapkv_decode_attend.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, P, SZ, P, P]
+        L.snapkv_status_string.restype = ctypes.c_char_p
+        L.snapkv_status_string.argtypes = [I32]
+        L.snapkv_abi_version.restype = I32
+        L.snapkv_abi_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def declared_functions() -> list:
+    """Names of the functions include/snapkv.h declares."""
+    text = open(_HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:[A-Za-z_][\w\s\*]*?)\b(snapkv_\w+)\s*\(", text, re.M)))
+
+
+def status_string(status: int) -> str:
+    return lib().snapkv_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> Optional[ctypes.c_void_p]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def make_params(*, batch, heads, head_dim, l_obs, l_prompt, pool_kernel, ratio_p=0.0, budget=0,
+                scope="prompt_causal", dtype=BF16) -> CompressParams:
+    return CompressParams(batch, heads, head_dim, l_obs, l_prompt, pool_kernel, _SCOPES[scope],
+                          float(ratio_p), int(budget), dtype, 0)
+
+
+def kept(params: CompressParams) -> int:
+    return int(lib().snapkv_compress_kept(ctypes.byref(params)))
+
+
+def compress_workspace_size(params: CompressParams) -> int:
+    return int(lib().snapkv_compress_workspace_size(ctypes.byref(params)))
+
+
+def decode_workspace_size(batch, heads, head_dim, cap) -> int:
+    return int(lib().snapkv_decode_workspace_size(batch, heads, head_dim, cap))
+
+
+def new_workspace(nbytes: int, device):
+    """A zero-filled workspace (the library leaves its counters zeroed for the next call)."""
+    import torch
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def compress(q_obs, k, v, *, pool_kernel, ratio_p=0.0, budget=0, scope="prompt_causal", cap=None,
+             k_out=None, v_out=None, len_out=None, idx_out=None, vote_out=None, want_idx=True,
+             want_vote=False, workspace=None, dev_status=None, stream=None):
+    """snapkv_compress on torch tensors q_obs [B,H,L_obs,d], k, v [B,H,L_prompt,d].
+
+    Returns a dict with k_out, v_out ([B,H,cap,d]), len_out [B], idx [B,H,k] (if wanted) and
+    vote [B,H,L_prefix] (if wanted), plus k (kept slots) and the workspace used.
+    """
+    import torch
+    B, H, L, d = k.shape
+    l_obs = q_obs.shape[2]
+    params = make_params(batch=B, heads=H, head_dim=d, l_obs=l_obs, l_prompt=L, pool_kernel=pool_kernel,
+                         ratio_p=ratio_p, budget=budget, scope=scope, dtype=_dtype_code(k))
+    ksel = kept(params)
+    if ksel < 0:
+        raise SnapKVError(ERR_INVALID_ARG, "snapkv_compress_kept")
+    if cap is None:
+        cap = ksel + l_obs
+    dev = k.device
+    if k_out is None:
+        k_out = torch.empty((B, H, cap, d), dtype=k.dtype, device=dev)
+    if v_out is None:
+        v_out = torch.empty((B, H, cap, d), dtype=k.dtype, device=dev)
+    if len_out is None:
+        len_out = torch.empty((B,), dtype=torch.int32, device=dev)
+    if idx_out is None and want_idx:
+        idx_out = torch.empty((B, H, max(ksel, 0)), dtype=torch.int32, device=dev)
+    if vote_out is None and want_vote:
+        vote_out = torch.empty((B, H, L - l_obs), dtype=torch.float32, device=dev)
+    need = compress_workspace_size(params)
+    if workspace is None:
+        workspace = new_workspace(need, dev)
+    for t in (q_obs, k, v, k_out, v_out):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    st = lib().snapkv_compress(ctypes.byref(params), _ptr(q_obs), _ptr(k), _ptr(v), _ptr(k_out), _ptr(v_out),
+                               int(cap), _ptr(len_out), _ptr(idx_out) if ksel > 0 else None, _ptr(vote_out),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                               _stream_handle(stream))
+    if st != OK:
+        raise SnapKVError(st, "snapkv_compress")
+    return {"k_out": k_out, "v_out": v_out, "len": len_out, "idx": idx_out, "vote": vote_out, "k": ksel,
+            "workspace": workspace, "cap": cap}
+
+
+def append(k_new, v_new, k_cache, v_cache, len_, *, dev_status=None, stream=None):
+    """snapkv_append: k_new, v_new [B,H,d] into k_cache, v_cache [B,H,cap,d] at row len[b]; len += 1."""
+    B, H, cap, d = k_cache.shape
+    st = lib().snapkv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), int(cap), _ptr(len_), B, H,
+                             d, _dtype_code(k_cache), _ptr(dev_status), _stream_handle(stream))
+    if st != OK:
+        raise SnapKVError(st, "snapkv_append")
+
+
+def decode_attend(q, k_cache, v_cache, len_, *, out=None, workspace=None, dev_status=None, stream=None):
+    """snapkv_decode_attend: q [B,H,d] over rows < len[b] of k_cache, v_cache [B,H,cap,d] -> out [B,H,d]."""
+    import torch
+    B, H, cap, d = k_cache.shape
+    if out is None:
+        out = torch.empty((B, H, d), dtype=k_cache.dtype, device=k_cache.device)
+    if workspace is None:
+        workspace = new_workspace(decode_workspace_size(B, H, d, cap), k_cache.device)
+    st = lib().snapkv_decode_attend(_ptr(q), _ptr(k_cache), _ptr(v_cache), int(cap), _ptr(len_), _ptr(out), B, H,
+                                    d, _dtype_code(k_cache), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                                    _stream_handle(stream))
+    if st != OK:
+        raise SnapKVError(st, "snapkv_decode_attend")
+    return out

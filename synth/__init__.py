@@ -91,7 +91,9 @@ def philox_block(ctr, key):
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """Widen bf16 bit patterns to the fp32 values they encode (exact)."""
-    return (bits.astype(np.uint32) << 16).view(np.float32)
+    pair = np.zeros(bits.shape + (2,), dtype=np.uint16)
+    pair[..., 1 if np.little_endian else 0] = bits
+    return pair.view(np.float32).reshape(bits.shape)
 
 
 def fill_host(B, H, rows, d, *, row0, seq0, head0, layer, tensor, seed, bf16,

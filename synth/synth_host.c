@@ -24,35 +24,34 @@ typedef struct {
   const float* chan_scale;
   const uint8_t* plant_mask;
   const float* plant_vec;
-  int head_begin, head_end; /* flattened (b, h) range of this worker */
+  int64_t row_begin, row_end; /* flattened ((b, h), r) row range of this worker */
 } fill_job;
 
-static void fill_heads(const fill_job* j) {
-  for (int bh = j->head_begin; bh < j->head_end; ++bh) {
-    const int b = bh / j->H, h = bh % j->H;
+static void fill_rows(const fill_job* j) {
+  const uint32_t s_hi = synth_stream_hi(j->layer, j->tensor);
+  for (int64_t fr = j->row_begin; fr < j->row_end; ++fr) {
+    const int64_t bh = fr / j->rows;
+    const int r = (int)(fr % j->rows);
+    const int b = (int)(bh / j->H), h = (int)(bh % j->H);
     const uint32_t s_lo = synth_stream_lo((uint32_t)(j->seq0 + b), (uint32_t)(j->head0 + h));
-    const uint32_t s_hi = synth_stream_hi(j->layer, j->tensor);
-    const size_t base = (size_t)bh * (size_t)j->rows * (size_t)j->d;
-    for (int r = 0; r < j->rows; ++r) {
-      const int planted = j->plant_mask ? (int)j->plant_mask[(size_t)bh * j->rows + r] : 0;
-      for (int c = 0; c < j->d; ++c) {
-        const uint32_t counter = (uint32_t)(j->row0 + r) * (uint32_t)j->d + (uint32_t)c;
-        const float scale = j->chan_scale ? j->chan_scale[(size_t)bh * j->d + c] : 1.0f;
-        const float plant = planted ? j->plant_vec[(size_t)bh * j->d + c] : 0.0f;
-        const float z = synth_element(j->seed, s_lo, s_hi, counter, j->chan_scale != NULL, scale,
-                                      planted, plant);
-        const size_t at = base + (size_t)r * j->d + c;
-        if (j->out_bf16)
-          ((uint16_t*)j->out)[at] = synth_bf16_rne(z);
-        else
-          ((float*)j->out)[at] = z;
-      }
+    const int planted = j->plant_mask ? (int)j->plant_mask[fr] : 0;
+    for (int c = 0; c < j->d; ++c) {
+      const uint32_t counter = (uint32_t)(j->row0 + r) * (uint32_t)j->d + (uint32_t)c;
+      const float scale = j->chan_scale ? j->chan_scale[bh * j->d + c] : 1.0f;
+      const float plant = planted ? j->plant_vec[bh * j->d + c] : 0.0f;
+      const float z = synth_element(j->seed, s_lo, s_hi, counter, j->chan_scale != NULL, scale, planted,
+                                    plant);
+      const size_t at = (size_t)fr * (size_t)j->d + (size_t)c;
+      if (j->out_bf16)
+        ((uint16_t*)j->out)[at] = synth_bf16_rne(z);
+      else
+        ((float*)j->out)[at] = z;
     }
   }
 }
 
 static void* fill_worker(void* arg) {
-  fill_heads((const fill_job*)arg);
+  fill_rows((const fill_job*)arg);
   return NULL;
 }
 
@@ -61,16 +60,16 @@ int synth_fill(void* out, int out_bf16, int B, int H, int rows, int d, int row0,
                const uint8_t* plant_mask, const float* plant_vec, int threads) {
   if (!out || B < 0 || H < 0 || rows < 0 || d <= 0) return 1;
   if (plant_mask && !plant_vec) return 1;
-  const int heads = B * H;
+  const int64_t total_rows = (int64_t)B * H * rows;
   if (threads < 1) threads = 1;
   if (threads > 64) threads = 64;
-  if (threads > heads) threads = heads > 0 ? heads : 1;
+  if ((int64_t)threads > total_rows / 64 + 1) threads = (int)(total_rows / 64 + 1);
   fill_job jobs[64];
   pthread_t tids[64];
   for (int t = 0; t < threads; ++t) {
     fill_job j = {out, out_bf16, B, H, rows, d, row0, seq0, head0, layer, tensor, seed,
                   chan_scale, plant_mask, plant_vec,
-                  (int)((long long)heads * t / threads), (int)((long long)heads * (t + 1) / threads)};
+                  total_rows * t / threads, total_rows * (t + 1) / threads};
     jobs[t] = j;
   }
   int started = 0;
@@ -78,9 +77,9 @@ int synth_fill(void* out, int out_bf16, int B, int H, int rows, int d, int row0,
     if (pthread_create(&tids[t], NULL, fill_worker, &jobs[t]) != 0) break;
     started = t;
   }
-  fill_heads(&jobs[0]);
+  fill_rows(&jobs[0]);
   for (int t = 1; t <= started; ++t) pthread_join(tids[t], NULL);
-  for (int t = started + 1; t < threads; ++t) fill_heads(&jobs[t]); /* threads that failed to start */
+  for (int t = started + 1; t < threads; ++t) fill_rows(&jobs[t]); /* threads that failed to start */
   return 0;
 }
 

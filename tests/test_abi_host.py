@@ -1,0 +1,108 @@
+"""Host-only checks of the C ABI: the library loads, exports every symbol include/snapkv.h
+declares, and rejects bad arguments on the host before any CUDA call (no GPU needed)."""
+import ctypes
+import subprocess
+
+import pytest
+
+from kv_cache_compression_gb300 import build as kbuild
+from kv_cache_compression_gb300 import snapkv as sk
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return sk.lib()
+
+
+def test_exports_every_declared_function(lib):
+    names = sk.declared_functions()
+    assert len(names) == 9
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", sk.library_path()], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(names) <= exported
+    assert lib.snapkv_abi_version() == 100
+
+
+def test_params_struct_layout():
+    assert ctypes.sizeof(sk.CompressParams) == 56
+    assert sk.CompressParams.l_prompt.offset == 16 and sk.CompressParams.ratio_p.offset == 32
+    assert sk.CompressParams.dtype.offset == 48
+
+
+def _params(**kw):
+    base = dict(batch=1, heads=4, head_dim=64, l_obs=32, l_prompt=1024, pool_kernel=7, ratio_p=0.05, budget=0,
+                scope="prompt_causal", dtype=sk.F32)
+    base.update(kw)
+    return sk.make_params(**base)
+
+
+def test_kept_slots_on_host(lib):
+    assert sk.kept(_params()) == 49                       # floor(0.05 * 992)
+    assert sk.kept(_params(budget=1024, l_prompt=16384)) == 1024
+    assert sk.kept(_params(budget=10 ** 9)) == 992        # budget beyond the prefix keeps everything
+    assert sk.kept(_params(ratio_p=1.0)) == 992
+    assert sk.kept(_params(ratio_p=0.0)) == 0
+    assert sk.kept(_params(l_prompt=32)) == -1             # L_obs must be < L_prompt
+    assert sk.kept(_params(pool_kernel=4)) == -1          # even kernel unsupported
+    assert sk.kept(_params(head_dim=96)) == -1
+    assert sk.kept(_params(ratio_p=1.5)) == -1
+    assert sk.kept(_params(ratio_p=float("nan"))) == -1
+
+
+def test_workspace_size_is_positive_and_monotone(lib):
+    a = sk.compress_workspace_size(_params())
+    b = sk.compress_workspace_size(_params(l_prompt=4096))
+    assert 0 < a < b and a % 256 == 0
+    assert sk.compress_workspace_size(_params(pool_kernel=2)) == 0
+    assert sk.decode_workspace_size(2, 4, 128, 1000) > 0
+    assert sk.decode_workspace_size(2, 4, 100, 1000) == 0
+
+
+def _call_compress(lib, params, **ptrs):
+    P = ctypes.c_void_p
+    good = {"q": 0x1000, "k": 0x100000, "v": 0x200000, "ko": 0x300000, "vo": 0x400000, "len": 0x500000,
+            "ws": 0x600000}
+    good.update(ptrs)
+    return lib.snapkv_compress(ctypes.byref(params), P(good["q"]), P(good["k"]), P(good["v"]), P(good["ko"]),
+                               P(good["vo"]), ptrs.get("cap", 81), P(good["len"]), None, None, P(good["ws"]),
+                               ptrs.get("ws_bytes", 1 << 30), None, None)
+
+
+def test_compress_rejects_bad_arguments_before_launch(lib):
+    p = _params()
+    assert lib.snapkv_compress(None, None, None, None, None, None, 81, None, None, None, None, 0, None, None) \
+        == sk.ERR_INVALID_ARG
+    assert _call_compress(lib, p, q=0) == sk.ERR_INVALID_ARG                  # NULL query
+    assert _call_compress(lib, p, k=0x100008) == sk.ERR_INVALID_ARG           # misaligned key pointer
+    assert _call_compress(lib, p, cap=80) == sk.ERR_CAPACITY                  # cap < k + L_obs
+    assert _call_compress(lib, p, ws=0) == sk.ERR_WORKSPACE
+    assert _call_compress(lib, p, ws_bytes=16) == sk.ERR_WORKSPACE
+    assert _call_compress(lib, p, ko=0x100000) == sk.ERR_INVALID_ARG          # output aliases input
+    assert _call_compress(lib, _params(pool_kernel=6)) == sk.ERR_UNSUPPORTED
+    assert _call_compress(lib, _params(head_dim=80)) == sk.ERR_UNSUPPORTED
+    assert _call_compress(lib, _params(l_obs=0)) == sk.ERR_INVALID_ARG
+    assert _call_compress(lib, _params(scope="prefix_only", dtype=7)) == sk.ERR_INVALID_ARG
+    bad = _params()
+    bad.reserved = 1
+    assert _call_compress(lib, bad) == sk.ERR_INVALID_ARG
+
+
+def test_decode_and_append_reject_bad_arguments(lib):
+    P = ctypes.c_void_p
+    assert lib.snapkv_append(None, P(16), P(32), P(48), 10, P(64), 1, 1, 64, 0, None, None) == sk.ERR_INVALID_ARG
+    assert lib.snapkv_append(P(16), P(32), P(48), P(64), 10, P(80), 1, 1, 72, 0, None, None) == sk.ERR_UNSUPPORTED
+    assert lib.snapkv_append(P(16), P(32), P(48), P(64), 0, P(80), 1, 1, 64, 0, None, None) == sk.ERR_INVALID_ARG
+    assert lib.snapkv_decode_attend(P(16), P(32), P(48), 10, P(64), P(80), 1, 1, 64, 0, None, 0, None, None) \
+        == sk.ERR_WORKSPACE
+    assert lib.snapkv_decode_attend(P(16), P(32), P(48), 10, P(64), P(88), 1, 1, 64, 0, P(256), 1 << 20, None,
+                                    None) == sk.ERR_INVALID_ARG               # misaligned output
+
+
+def test_status_strings(lib):
+    assert sk.status_string(0) == "SNAPKV_OK"
+    assert sk.status_string(4) == "SNAPKV_ERR_CAPACITY"
+    assert sk.status_string(4 | 16).startswith("SNAPKV_ERR_TIMEOUT")
+    assert sk.status_string(-3) == "SNAPKV_ERR_UNKNOWN"

@@ -1,0 +1,138 @@
+"""GPU parity of snapkv_compress against the CPU oracle, through the C ABI.
+
+Inputs are generated on the device by the seeded generator and regenerated bit-identically on
+the host for the oracle. Every workload of the benchmark suite is covered: the tiny fp32 case and
+the Llama-2-7B-shaped layer on every head, the long-context case, the 32-layer batch-8 prefill and
+the ragged-prompt decode workload on seeded samples, plus edge cases (k = 0, k = L_prefix, L_obs = 1,
+odd tails, both softmax scopes, several batches, exact ties).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import snapkv_oracle as orc
+from tests.parity import check_compress_head, to_numpy_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev(gpu_device):
+    import __graft_entry__
+    __graft_entry__.build()
+    return gpu_device
+
+
+def _run_workload(dev, wl, layer=0, seq0=0, nseq=None, l_prompt=None, heads=None, scope="prompt_causal"):
+    from kv_cache_compression_gb300 import snapkv
+    nseq = nseq if nseq is not None else wl.batch
+    L = l_prompt if l_prompt is not None else wl.prompt_lengths()[seq0]
+    q, k, v, _ = synth.device_inputs(wl, layer, seq0, nseq, L, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, ratio_p=wl.ratio_p, budget=wl.budget, scope=scope,
+                          want_vote=True, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    l_prefix = L - wl.l_obs
+    ksel = res["k"]
+    assert res["len"].cpu().tolist() == [ksel + wl.l_obs] * nseq
+    excused = 0
+    for b in range(nseq):
+        for h in (heads if heads is not None else range(wl.heads)):
+            hi = synth.host_head(wl, layer, seq0 + b, h, l_prompt=L)
+            ref = orc.compress_head(hi.q_obs, hi.k, hi.v, pool_kernel=wl.pool_kernel, ratio_p=wl.ratio_p,
+                                    budget=wl.budget, scope=scope)
+            rep = check_compress_head(gpu_idx=res["idx"][b, h].cpu().numpy(),
+                                      gpu_kc=to_numpy_f32(res["k_out"][b, h]), gpu_vc=to_numpy_f32(res["v_out"][b, h]),
+                                      gpu_vote=res["vote"][b, h].cpu().numpy(), ref=ref, k_in=hi.k, v_in=hi.v,
+                                      l_prefix=l_prefix, l_obs=wl.l_obs, where=f"layer {layer} seq {seq0 + b} head {h}")
+            excused += rep.excused
+    return res, excused
+
+
+def test_tiny_fp32_every_head(dev):
+    _, excused = _run_workload(dev, synth.WORKLOADS[0])
+    assert excused == 0
+
+
+def test_tiny_fp32_prefix_only_scope(dev):
+    _run_workload(dev, synth.WORKLOADS[0], scope="prefix_only")
+
+
+def test_llama_layer_every_head(dev):
+    _, excused = _run_workload(dev, synth.WORKLOADS[1])
+    print(f"boundary-excused indices: {excused}")
+
+
+def test_long_context_sampled_heads(dev):
+    _run_workload(dev, synth.WORKLOADS[3], heads=[0, 13, 31])
+
+
+def test_prefill_32_layers_sampled(dev):
+    wl = synth.WORKLOADS[2]
+    rng = np.random.default_rng(2)
+    for layer in (0, 31, int(rng.integers(1, 31))):
+        _run_workload(dev, wl, layer=layer, seq0=int(rng.integers(0, 8)), nseq=1,
+                      heads=sorted(rng.choice(32, 3, replace=False).tolist()))
+
+
+def test_ragged_prompts_sampled(dev):
+    wl = synth.WORKLOADS[4]
+    lens = wl.prompt_lengths()
+    for seq in (int(np.argmin(lens)), int(np.argmax(lens)), 17):
+        _run_workload(dev, wl, layer=seq % 32, seq0=seq, nseq=1, heads=[0, 31])
+
+
+EDGE_CASES = [
+    # (bf16, d, l_obs, pool, l_prompt, ratio_p, budget, scope, batch, heads)
+    (False, 64, 1, 1, 37, 0.5, 0, "prompt_causal", 1, 1),
+    (True, 128, 16, 5, 1000, 0.0, 100, "prefix_only", 1, 2),
+    (True, 64, 64, 13, 3001, 0.05, 0, "prompt_causal", 1, 3),
+    (True, 128, 128, 3, 2049, 1.0, 0, "prompt_causal", 1, 2),
+    (False, 128, 32, 7, 1025, 0.0, 0, "prompt_causal", 2, 2),
+    (True, 128, 8, 9, 65, 0.0, 10000, "prompt_causal", 1, 1),
+    (True, 128, 32, 7, 777, 0.2, 0, "prompt_causal", 3, 5),
+    (False, 64, 48, 15, 4099, 0.03, 0, "prefix_only", 2, 2),
+]
+
+
+@pytest.mark.parametrize("case", EDGE_CASES, ids=lambda c: f"bf16={c[0]}-d{c[1]}-obs{c[2]}-K{c[3]}-L{c[4]}")
+def test_edge_cases(dev, case):
+    bf16, d, l_obs, pool, L, p, budget, scope, B, H = case
+    wl = synth.Workload("edge", 40 + L % 17, bf16=bf16, batch=B, heads=H, head_dim=d, layers=1, l_prompt=L,
+                        l_obs=l_obs, pool_kernel=pool, ratio_p=p, budget=budget)
+    _run_workload(dev, wl, scope=scope)
+
+
+def test_zero_queries_keep_the_first_k(dev):
+    """q = 0 makes every pooled score equal; ties go to the lower index, so I = 0..k-1 exactly."""
+    from kv_cache_compression_gb300 import snapkv
+    B, H, L, lo, d = 1, 3, 3000, 32, 128
+    k = torch.randn(B, H, L, d, generator=torch.Generator().manual_seed(0)).to(torch.bfloat16).to(dev)
+    q = torch.zeros(B, H, lo, d, dtype=torch.bfloat16, device=dev)
+    res = snapkv.compress(q, k, k.clone(), pool_kernel=7, budget=300)
+    torch.cuda.synchronize()
+    for h in range(H):
+        assert res["idx"][0, h].cpu().tolist() == list(range(300))
+
+
+def test_workspace_is_reusable(dev):
+    from kv_cache_compression_gb300 import snapkv
+    wl = synth.WORKLOADS[1].with_(heads=4, l_prompt=4096)
+    q, k, v, _ = synth.device_inputs(wl, 0, 0, 1, wl.l_prompt, dev)
+    first = snapkv.compress(q, k, v, pool_kernel=7, budget=wl.budget, want_vote=True)
+    again = snapkv.compress(q, k, v, pool_kernel=7, budget=wl.budget, want_vote=True, workspace=first["workspace"])
+    torch.cuda.synchronize()
+    assert torch.equal(first["idx"], again["idx"])
+    assert torch.equal(first["vote"], again["vote"])
+    assert torch.equal(first["k_out"], again["k_out"])
+
+
+def test_device_generator_matches_host(dev):
+    wl = synth.WORKLOADS[2]
+    q, k, v, _ = synth.device_inputs(wl, 5, 3, 1, 2048, dev)
+    hi = synth.host_head(wl, 5, 3, 7, l_prompt=2048)
+    assert np.array_equal(to_numpy_f32(k[0, 7]), hi.k)
+    assert np.array_equal(to_numpy_f32(v[0, 7]), hi.v)
+    assert np.array_equal(to_numpy_f32(q[0, 7]), hi.q_obs)

@@ -1,0 +1,134 @@
+"""GPU parity of snapkv_append + snapkv_decode_attend against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import snapkv_oracle as orc
+from tests.parity import check_decode, to_numpy_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev(gpu_device):
+    import __graft_entry__
+    __graft_entry__.build()
+    return gpu_device
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 128),
+                                     (torch.float32, 64)])
+def test_decode_ragged_lengths(dev, dtype, d):
+    from kv_cache_compression_gb300 import snapkv
+    g = torch.Generator().manual_seed(d)
+    B, H, cap = 5, 3, 700
+    lens = [1, 255, 256, 699, 700]
+    kc = torch.randn(B, H, cap, d, generator=g).to(dtype)
+    vc = torch.randn(B, H, cap, d, generator=g).to(dtype)
+    q = (torch.randn(B, H, d, generator=g) * 2).to(dtype)
+    length = torch.tensor(lens, dtype=torch.int32)
+    out = snapkv.decode_attend(q.to(dev), kc.to(dev), vc.to(dev), length.to(dev))
+    torch.cuda.synchronize()
+    o = to_numpy_f32(out)
+    for b in range(B):
+        for h in range(H):
+            n = lens[b]
+            ref = orc.decode_attend(q[b, h].float().numpy(), kc[b, h, :n].float().numpy(), vc[b, h, :n].float().numpy())
+            check_decode(o[b, h], ref, dtype == torch.bfloat16, where=f"b{b} h{h} n{n}")
+
+
+def test_decode_zero_length_gives_zero_and_overlong_is_reported(dev):
+    from kv_cache_compression_gb300 import snapkv
+    B, H, cap, d = 2, 2, 64, 128
+    kc = torch.randn(B, H, cap, d, device=dev).to(torch.bfloat16)
+    vc = torch.randn(B, H, cap, d, device=dev).to(torch.bfloat16)
+    q = torch.randn(B, H, d, device=dev).to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = snapkv.decode_attend(q, kc, vc, torch.tensor([0, cap + 5], dtype=torch.int32, device=dev),
+                               dev_status=status)
+    torch.cuda.synchronize()
+    assert torch.all(out[0] == 0)
+    assert int(status.item()) & snapkv.ERR_CAPACITY
+    full = snapkv.decode_attend(q, kc, vc, torch.tensor([cap, cap], dtype=torch.int32, device=dev))
+    torch.cuda.synchronize()
+    assert torch.equal(out[1], full[1])     # clamped to the capacity
+
+
+def test_append_writes_row_and_advances_length(dev):
+    from kv_cache_compression_gb300 import snapkv
+    B, H, cap, d = 3, 4, 10, 64
+    kc = torch.zeros(B, H, cap, d, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    length = torch.tensor([0, 5, cap], dtype=torch.int32, device=dev)
+    kn = torch.randn(B, H, d, device=dev).to(torch.bfloat16)
+    vn = torch.randn(B, H, d, device=dev).to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    snapkv.append(kn, vn, kc, vc, length, dev_status=status)
+    torch.cuda.synchronize()
+    assert length.cpu().tolist() == [1, 6, cap]          # the full sequence is left as it was
+    assert int(status.item()) == snapkv.ERR_CAPACITY
+    assert torch.equal(kc[0, :, 0], kn[0]) and torch.equal(vc[1, :, 5], vn[1])
+    assert torch.count_nonzero(kc[2]) == 0
+    assert torch.count_nonzero(kc[0, :, 1:]) == 0
+
+
+def test_uncompressed_cache_decode_equals_full_causal_attention(dev):
+    """KV-cache chapter 22.7 on the GPU: with k = L_prefix the compressed cache is the whole prompt,
+    and append + decode of each new token gives the oracle's cached-decode rows (which the oracle's
+    own pin equates with full causal attention)."""
+    from kv_cache_compression_gb300 import snapkv
+    wl = synth.WORKLOADS[1].with_(heads=2, l_prompt=640, budget=0, ratio_p=1.0, plants=0)
+    steps = 6
+    q, k, v, _ = synth.device_inputs(wl, 0, 0, 1, wl.l_prompt, dev)
+    res = snapkv.compress(q, k, v, pool_kernel=7, ratio_p=1.0, cap=wl.l_prompt + steps)
+    outs = []
+    for t in range(steps):
+        qn, kn, vn = synth.device_decode_tokens(wl, 0, t, 0, 1, dev)
+        snapkv.append(kn, vn, res["k_out"], res["v_out"], res["len"])
+        outs.append(snapkv.decode_attend(qn, res["k_out"], res["v_out"], res["len"]))
+    torch.cuda.synchronize()
+    assert res["len"].item() == wl.l_prompt + steps
+    for h in range(wl.heads):
+        hi = synth.host_head(wl, 0, 0, h)
+        kc, vc = hi.k, hi.v
+        for t in range(steps):
+            qn, kn, vn = synth.host_decode_token(wl, 0, 0, h, t)
+            kc, vc = orc.append(kc, vc, kn, vn)
+            check_decode(to_numpy_f32(outs[t][0, h]), orc.decode_attend(qn, kc, vc), True, where=f"h{h} t{t}")
+
+
+def test_compressed_decode_workload_sampled(dev):
+    """The ragged-prompt decode workload on sampled (sequence, layer): compress into a cache of
+    capacity 2048 + L_obs + 128, then all 128 decode steps of append + attention, checked against
+    the oracle re-simulating compression and every step on sampled heads."""
+    from kv_cache_compression_gb300 import snapkv
+    wl = synth.WORKLOADS[4]
+    lens = wl.prompt_lengths()
+    cap = wl.budget + wl.l_obs + wl.decode_steps
+    for seq, layer, heads in ((3, 0, [0, 17]), (int(np.argmax(lens)), 31, [31])):
+        L = lens[seq]
+        q, k, v, _ = synth.device_inputs(wl, layer, seq, 1, L, dev)
+        res = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, budget=wl.budget, cap=cap)
+        del q, k, v
+        ws = snapkv.new_workspace(snapkv.decode_workspace_size(1, wl.heads, wl.head_dim, cap), dev)
+        outs = []
+        for t in range(wl.decode_steps):
+            qn, kn, vn = synth.device_decode_tokens(wl, layer, t, seq, 1, dev)
+            snapkv.append(kn, vn, res["k_out"], res["v_out"], res["len"])
+            outs.append(snapkv.decode_attend(qn, res["k_out"], res["v_out"], res["len"], workspace=ws)[0, heads].cpu())
+        torch.cuda.synchronize()
+        assert res["len"].item() == cap
+        for j, h in enumerate(heads):
+            hi = synth.host_head(wl, layer, seq, h, l_prompt=L)
+            ref = orc.compress_head(hi.q_obs, hi.k, hi.v, pool_kernel=wl.pool_kernel, budget=wl.budget)
+            got_idx = res["idx"][0, h].cpu().numpy()
+            # decode continues from the GPU's own kept set (identical unless a boundary tie flipped)
+            kc, vc = orc.gather_with_window(hi.k, got_idx, L - wl.l_obs), orc.gather_with_window(hi.v, got_idx, L - wl.l_obs)
+            assert np.setxor1d(got_idx, ref.idx).size == 0 or \
+                np.all(np.abs(ref.p[np.setxor1d(got_idx, ref.idx)] - ref.tau) <= 1e-5 * ref.tau)
+            for t in range(wl.decode_steps):
+                qn, kn, vn = synth.host_decode_token(wl, layer, seq, h, t)
+                kc, vc = orc.append(kc, vc, kn, vn)
+                check_decode(to_numpy_f32(outs[t][j]), orc.decode_attend(qn, kc, vc), True,
+                             where=f"seq {seq} layer {layer} head {h} step {t}")

@@ -312,6 +312,9 @@ def run_ours(args, rank, world, local_rank):
 
     # One event set per timed step: the four compress stages (recorded inside the library), then decode.
     step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev + 2)] for _ in range(args.steps)]
+    for evs in step_events:      # torch creates its events lazily: record once so each has a handle
+        for e in evs:
+            e.record(stream)
 
     for i in range(args.warmup):
         launch_step(i)

@@ -169,6 +169,29 @@ SNAPKV_API snapkv_status snapkv_decode_attend(const void* q, const void* k_cache
                                    size_t workspace_bytes, int32_t* dev_status,
                                    snapkv_stream_t stream);
 
+/*
+ * snapkv_decode_attend_noalloc — snapkv_decode_attend without a workspace argument, for callers
+ * that cannot allocate device memory or hand one over: for example a plugin or custom-operator
+ * interface that passes only inputs and outputs, or a latency-critical serving loop where a
+ * cudaMalloc (which can synchronise the device and take a driver-wide lock) is not allowed.
+ * The pages have no counterpart to this entry point; it computes exactly what
+ * snapkv_decode_attend computes, with the same arguments minus the workspace.
+ *
+ * It allocates nothing. Its scratch (the split partials and the per-head tickets) is a 16 MiB
+ * array built into the library, which every GPU that loads the library holds until the process
+ * exits. A problem needing more than that — 256-byte-rounded B*H*ceil(cap/256)*(d+2)*4 bytes of
+ * partials plus B*H*4 bytes of tickets — is rejected with SNAPKV_ERR_WORKSPACE before anything
+ * is enqueued. The first call on a device looks up the array's device address (once per device,
+ * with that device current), so make that first call before any stream capture. Every call
+ * shares the one array and it keeps the last call's contents (the tickets are cleared on `stream`
+ * at the start of each call), so calls that overlap on the GPU — on different streams, or from
+ * different host threads — race and give wrong results: serialise them.
+ */
+SNAPKV_API snapkv_status snapkv_decode_attend_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                                      int64_t cap, const int32_t* len, void* out, int32_t batch,
+                                                      int32_t heads, int32_t head_dim, int32_t dtype,
+                                                      int32_t* dev_status, snapkv_stream_t stream);
+
 /* Human-readable name of a status value (a static string; bits are listed when several). */
 SNAPKV_API const char* snapkv_status_string(int32_t status);
 

@@ -244,4 +244,38 @@ snapkv_status snapkv_decode_attend(const void* q, const void* k_cache, const voi
   return SNAPKV_OK;
 }
 
+snapkv_status snapkv_decode_attend_noalloc(const void* q, const void* k_cache, const void* v_cache, int64_t cap,
+                                           const int32_t* len, void* out, int32_t batch, int32_t heads,
+                                           int32_t head_dim, int32_t dtype, int32_t* dev_status,
+                                           snapkv_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !len || !out) return SNAPKV_ERR_INVALID_ARG;
+  if (batch < 1 || heads < 1 || head_dim < 1 || cap < 1 || cap > kMaxPrompt) return SNAPKV_ERR_INVALID_ARG;
+  if (dtype != SNAPKV_F32 && dtype != SNAPKV_BF16) return SNAPKV_ERR_INVALID_ARG;
+  if ((int64_t)batch * heads > 65535) return SNAPKV_ERR_INVALID_ARG;  // grid.y limit
+  if (head_dim != 64 && head_dim != 128) return SNAPKV_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || ((uintptr_t)len & 3u) ||
+      ((uintptr_t)dev_status & 3u))
+    return SNAPKV_ERR_INVALID_ARG;
+  if (decode_layout(batch, heads, head_dim, cap).total > kDecodeNoAllocScratchBytes) return SNAPKV_ERR_WORKSPACE;
+  DecodeJob job;
+  job.batch = batch;
+  job.heads = heads;
+  job.head_dim = head_dim;
+  job.dtype = dtype;
+  job.cap = cap;
+  job.q = q;
+  job.k_cache = k_cache;
+  job.v_cache = v_cache;
+  job.len = len;
+  job.out = out;
+  job.partial = nullptr;
+  job.tickets = nullptr;
+  job.split_rows = 0;
+  job.n_split = 0;
+  job.dev_status = dev_status;
+  job.stream = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_decode_noalloc(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  return SNAPKV_OK;
+}
+
 }  // extern "C"

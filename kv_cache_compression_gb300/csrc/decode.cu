@@ -6,8 +6,15 @@
 // split keeps an online softmax (running max m, running sum l, unnormalised output o) in the log2
 // domain, writes (m, l, o) to the workspace, and the last CTA of the head to finish (an atomic
 // ticket, no waiting) merges the splits and writes o / l.
+#include <mutex>
+
 #include "snapkv_common.cuh"
 #include "snapkv_internal.h"
+
+// Built-in scratch of snapkv_decode_attend_noalloc: the split partials and the per-head tickets
+// that snapkv_decode_attend otherwise takes from the caller's workspace. Every GPU that loads the
+// library holds this array until the process exits; all calls of that entry point share it.
+static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[snapkv::kDecodeNoAllocScratchBytes];
 
 namespace snapkv {
 namespace {
@@ -233,6 +240,47 @@ cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, v
                                            static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), cap, len,
                                            heads, vpr, dev_status);
   return cudaGetLastError();
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the built-in scratch on the current device. The first call on a device looks
+// it up (the array's host-side name is only a stand-in, never a device address) and caches it.
+cudaError_t noalloc_scratch_address(void** out) {
+  int dev = -1;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+    if (err != cudaSuccess) return err;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_decode_noalloc(DecodeJob job) {
+  const DecodeLayout L = decode_layout(job.batch, job.heads, job.head_dim, job.cap);
+  if (L.total > kDecodeNoAllocScratchBytes) return cudaErrorInvalidValue;  // rejected earlier by the ABI
+  void* base = nullptr;
+  cudaError_t err = noalloc_scratch_address(&base);
+  if (err != cudaSuccess) return err;
+  char* ws = static_cast<char*>(base);
+  job.partial = reinterpret_cast<float*>(ws + L.partial);
+  job.tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
+  job.split_rows = L.split_rows;
+  job.n_split = L.n_split;
+  // The array keeps whatever the last call left; the tickets must start at zero.
+  err = cudaMemsetAsync(job.tickets, 0, (size_t)job.batch * job.heads * sizeof(uint32_t), job.stream);
+  if (err != cudaSuccess) return err;
+  return launch_decode(job);
 }
 
 cudaError_t launch_decode(const DecodeJob& job) {

@@ -75,4 +75,10 @@ cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, v
                           int32_t* dev_status, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeJob& job);
 
+// Size of the built-in scratch array behind snapkv_decode_attend_noalloc.
+constexpr size_t kDecodeNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB
+// Decode attention with the split partials and tickets in the built-in scratch array
+// (job.partial / job.tickets are ignored and replaced).
+cudaError_t launch_decode_noalloc(DecodeJob job);
+
 }  // namespace snapkv

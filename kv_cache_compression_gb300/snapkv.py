@@ -71,6 +71,8 @@ def lib():
         L.snapkv_decode_workspace_size.argtypes = [I32, I32, I32, I64]
         L.snapkv_decode_attend.restype = I32
         L.snapkv_decode_attend.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, P, SZ, P, P]
+        L.snapkv_decode_attend_noalloc.restype = I32
+        L.snapkv_decode_attend_noalloc.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, P, P]
         L.snapkv_status_string.restype = ctypes.c_char_p
         L.snapkv_status_string.argtypes = [I32]
         L.snapkv_abi_version.restype = I32

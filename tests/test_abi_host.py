@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = sk.declared_functions()
-    assert len(names) == 9
+    assert len(names) == 10
     for n in names:
         assert hasattr(lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", sk.library_path()], capture_output=True, text=True).stdout

@@ -65,6 +65,14 @@ typedef enum { SNAPKV_F32 = 0, SNAPKV_BF16 = 1 } snapkv_dtype;
  *                  (アルゴリズム) normalises them. */
 typedef enum { SNAPKV_SCOPE_PROMPT_CAUSAL = 0, SNAPKV_SCOPE_PREFIX_ONLY = 1 } snapkv_softmax_scope;
 
+/* Which kernels compute the logits, softmax statistics and vote (the results agree within the
+ * vote tolerance; the selection and the gathered rows are the same up to top-k boundary ties):
+ *   AUTO:        the tensor-core kernel when eligible (bf16, L_obs <= 64, at most 2 x SMs items
+ *                per head), else the SIMT kernels;
+ *   SIMT:        always the SIMT fp32 kernels (any dtype, L_obs <= 128);
+ *   TENSOR_CORE: the tensor-core kernel, or SNAPKV_ERR_UNSUPPORTED when not eligible. */
+typedef enum { SNAPKV_ALGO_AUTO = 0, SNAPKV_ALGO_SIMT = 1, SNAPKV_ALGO_TENSOR_CORE = 2 } snapkv_algo;
+
 /* Problem statement of one compression call: one layer, `batch` sequences of one length. */
 typedef struct {
   int32_t batch;          /* B >= 1                                                           */
@@ -77,7 +85,7 @@ typedef struct {
   double ratio_p;         /* p in [0,1]: k = floor(p * L_prefix) in IEEE double (budget <= 0)  */
   int64_t budget;         /* > 0: k = min(budget, L_prefix) (the listing's max_cap)            */
   int32_t dtype;          /* snapkv_dtype of Q, K, V and of the outputs                         */
-  int32_t reserved;       /* must be 0                                                          */
+  int32_t algo;           /* snapkv_algo (0 = automatic choice)                                 */
 } snapkv_compress_params;
 
 /* Kept prefix slots per head, k (host-side, for sizing). Returns -1 if the params are invalid. */

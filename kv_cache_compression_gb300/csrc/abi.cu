@@ -33,7 +33,8 @@ snapkv_status check_params(const snapkv_compress_params* p, int64_t* l_prefix, i
   if (p->softmax_scope != SNAPKV_SCOPE_PROMPT_CAUSAL && p->softmax_scope != SNAPKV_SCOPE_PREFIX_ONLY)
     return SNAPKV_ERR_INVALID_ARG;
   if (p->dtype != SNAPKV_F32 && p->dtype != SNAPKV_BF16) return SNAPKV_ERR_INVALID_ARG;
-  if (p->reserved != 0) return SNAPKV_ERR_INVALID_ARG;
+  if (p->algo != SNAPKV_ALGO_AUTO && p->algo != SNAPKV_ALGO_SIMT && p->algo != SNAPKV_ALGO_TENSOR_CORE)
+    return SNAPKV_ERR_INVALID_ARG;
   if (p->budget <= 0 && !(p->ratio_p >= 0.0 && p->ratio_p <= 1.0)) return SNAPKV_ERR_INVALID_ARG;
   if ((int64_t)p->batch * p->heads > 65535) return SNAPKV_ERR_INVALID_ARG;  // grid.y limit
   if (p->head_dim != 64 && p->head_dim != 128) return SNAPKV_ERR_UNSUPPORTED;
@@ -61,11 +62,15 @@ CompressLayout compress_layout(int batch, int heads, int l_obs, int64_t l_prompt
   L.vote_chunk = kVoteChunk;
   L.n_chunk_all = (int)((l_prompt + kVoteChunk - 1) / kVoteChunk);
   L.n_chunk_prefix = (int)((l_prefix + kVoteChunk - 1) / kVoteChunk);
+  const int64_t tc_items = (l_prompt + vote_tc_keys_per_item(l_obs) - 1) / vote_tc_keys_per_item(l_obs);
+  const int64_t chunks = tc_items > L.n_chunk_all ? tc_items : L.n_chunk_all;
   L.partial = 0;
-  L.c = up256(bh * L.n_chunk_all * l_obs * 2 * sizeof(float));
+  L.c = up256(bh * chunks * l_obs * 2 * sizeof(float));
   L.p = L.c + up256(bh * l_prefix * sizeof(float));
   L.idx = L.p + up256(bh * l_prefix * sizeof(float));
-  L.total = L.idx + up256(bh * (k_sel > 0 ? k_sel : 1) * sizeof(int32_t));
+  L.tc_zsum = L.idx + up256(bh * (k_sel > 0 ? k_sel : 1) * sizeof(int32_t));
+  L.tc_counters = L.tc_zsum + up256(bh * l_obs * sizeof(double));
+  L.total = L.tc_counters + up256((bh + 1) * sizeof(uint32_t));
   return L;
 }
 
@@ -163,6 +168,9 @@ snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, con
   job.c = vote_out ? vote_out : reinterpret_cast<float*>(ws + L.c);
   job.p = reinterpret_cast<float*>(ws + L.p);
   job.partial = reinterpret_cast<float*>(ws + L.partial);
+  job.tc_zsum = reinterpret_cast<double*>(ws + L.tc_zsum);
+  job.tc_cnt = reinterpret_cast<uint32_t*>(ws + L.tc_counters);
+  job.tc_done = job.tc_cnt + bh;
   job.vote_chunk = L.vote_chunk;
   job.n_chunk_all = L.n_chunk_all;
   job.n_chunk_prefix = L.n_chunk_prefix;
@@ -171,7 +179,18 @@ snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, con
   job.events = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(stage_events));
   job.n_events = n_events;
 
-  if (launch_vote_simt(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  const bool tc_ok = vote_tc_eligible(job);
+  if (params->algo == SNAPKV_ALGO_TENSOR_CORE && !tc_ok) return SNAPKV_ERR_UNSUPPORTED;
+  bool voted = false;
+  if (tc_ok && params->algo != SNAPKV_ALGO_SIMT) {
+    if (launch_vote_tc(job) == cudaSuccess) {
+      voted = true;
+    } else {
+      cudaGetLastError();   // a refused cooperative launch is not sticky; use the SIMT kernels
+      if (params->algo == SNAPKV_ALGO_TENSOR_CORE) return SNAPKV_ERR_CUDA;
+    }
+  }
+  if (!voted && launch_vote_simt(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
   if (launch_pool_topk(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
   if (launch_gather(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
   return SNAPKV_OK;

@@ -21,6 +21,9 @@ struct CompressJob {
   float* c;            // vote (caller's buffer or workspace)
   float* p;            // pooled vote (workspace)
   float* partial;      // per-chunk row statistics (workspace)
+  double* tc_zsum;     // per-(head, row) fp64 sums of 2^(logit) (workspace, zero between calls)
+  uint32_t* tc_cnt;    // per-head statistics items done (workspace, zero between calls)
+  uint32_t* tc_done;   // CTAs finished (workspace, zero between calls)
   int vote_chunk;      // keys per chunk of the score/vote kernels
   int n_chunk_all;     // chunks covering the whole prompt
   int n_chunk_prefix;  // chunks covering the prefix
@@ -38,13 +41,17 @@ enum { kStageScore = 0, kStageVote = 1, kStageTopk = 2, kStageGather = 3, kStage
 
 // Workspace layout of a compression call (byte offsets, each 256-aligned).
 struct CompressLayout {
-  size_t partial, c, p, idx, total;
+  size_t partial, c, p, idx, tc_zsum, tc_counters, total;
   int vote_chunk, n_chunk_all, n_chunk_prefix;
 };
 
 CompressLayout compress_layout(int batch, int heads, int l_obs, int64_t l_prompt, int64_t k_sel);
 
 cudaError_t launch_vote_simt(const CompressJob& job);
+// Tensor-core score + vote (bf16, d 64/128, L_obs <= 64, items per head <= 2 x SMs).
+bool vote_tc_eligible(const CompressJob& job);
+int vote_tc_keys_per_item(int l_obs);
+cudaError_t launch_vote_tc(const CompressJob& job);
 cudaError_t launch_pool_topk(const CompressJob& job);
 cudaError_t launch_gather(const CompressJob& job);
 

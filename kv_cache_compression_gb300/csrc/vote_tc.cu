@@ -1,0 +1,722 @@
+// Score + softmax + vote on the 5th-generation tensor cores (bf16, d = 64 or 128, L_obs <= 64).
+//
+// SnapKV explainer ("論文解説: SnapKV"), sections 投票メカニズム and アルゴリズム: logits
+// s_ij = q_i . k_j / sqrt(d) of the L_obs window queries against every prompt key, the row
+// softmax w_ij = exp(s_ij - m_i) / Z_i, and the vote C_j = sum_i w_ij over the prefix keys.
+//
+// Work is a queue of items, each TI = 128 / N tiles of 128 keys of one head, of two kinds:
+//   A (statistics): per window row, the maximum M of the logits (log2 domain) over the item's
+//     visible keys and z = sum 2^(s' - M); the item adds z * 2^M into the head's fp64 row sum
+//     Z_i = sum_j 2^(s'_ij) (a fire-and-forget reduction) and then bumps the head's counter with a
+//     release-ordered reduction. fp64's exponent range holds every row maximum within +-1000 in
+//     log2 units; a larger one is reported as SNAPKV_ERR_UNSUPPORTED.
+//   B (vote): once the head's counter shows all its A items, C_j = sum_i 2^(s'_ij - log2 Z_i) for
+//     the item's prefix keys (the softmax max-subtraction cancels between numerator and Z_i).
+// Resident mode (when a head has at most 4 x grid items): the queue holds one item per key chunk;
+// its logits stay in its TMEM slot after the statistics pass, and the warpgroup computes the vote
+// from TMEM once the head is complete, so each key is read by the SM only once. With at most grid
+// items per head a CTA holds at most one item of a head, and the vote follows its own statistics
+// at once; otherwise it follows the statistics of the group's next item, so that a warpgroup never
+// waits while holding an item without pass A: a CTA holds at most four items, two per warpgroup,
+// and at most four items of one head, so the lowest unfinished head always completes.
+//
+// A persistent, cooperative grid (one CTA per SM) takes queue positions round-robin. Per CTA:
+//   warp 0      TMA: streams each item's key tiles (128 keys x 128 B per box, 128-byte swizzle)
+//               into a ring of shared-memory stages and the head's window queries into one of two
+//               buffers;
+//   warp 1      MMA: one thread issues tcgen05.mma (M = 128 keys, N = padded L_obs, K = 16) for each
+//               tile into the item's TMEM slot (four slots of 128 columns);
+//   warps 2..9  epilogue: two warpgroups, one thread per key (TMEM lane); warpgroup g takes the
+//               CTA's items n = g, g + 2, ..., reads their logits with tcgen05.ld and gives the slot
+//               back as soon as it has read it.
+//
+// Progress: A items never wait, and a B item waits only for A items that come earlier in the queue;
+// every CTA takes its positions in queue order and the cooperative launch keeps all CTAs resident,
+// so the lowest unfinished head always completes. All waits are bounded; on a timeout the kernel
+// reports SNAPKV_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "sm100_ptx.cuh"
+#include "snapkv_common.cuh"
+#include "snapkv_internal.h"
+
+namespace snapkv {
+namespace {
+
+constexpr int kEpiWarps = 8;                       // two warpgroups of epilogue warps
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreadsTc = 64 + kEpiThreads;
+constexpr int kTileKeys = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clock
+constexpr long long kDrainLimit = 400000000LL;
+
+struct TcArgs {
+  int64_t l_prompt, l_prefix;
+  int l_obs, scope, n_chunk, n_queue, keys_per_item, bh_total, delta;
+  int resident;      // 1: one item per key chunk, logits stay in TMEM from statistics to vote
+  float scale_log2;
+  double* zsum;      // [BH][l_obs]: Z_i = sum_j 2^(s'_ij) over the head's visible keys (fp64)
+  uint32_t* cnt;     // [BH] A items whose contribution to zsum is complete
+  uint32_t* done;    // [1] CTAs finished
+  float* c_out;      // [BH][l_prefix]
+  int32_t* dev_status;
+};
+
+struct Item {
+  int kind;   // 0: statistics (A), 1: vote (B)
+  int head;
+  int chunk;
+};
+
+// Queue position -> item. Blocks of n_chunk positions: A(0..delta-1), then B(h), A(h + delta)
+// alternating, then the last B heads.
+__device__ __forceinline__ Item queue_item(const TcArgs& a, int p) {
+  const int nc = a.n_chunk, H = a.bh_total, D = a.delta;
+  const int blk = p / nc, off = p % nc;
+  Item it;
+  it.chunk = off;
+  if (a.resident) {   // every item is a statistics item whose vote follows from TMEM
+    it.kind = 0;
+    it.head = blk;
+    return it;
+  }
+  if (blk < D) {
+    it.kind = 0;
+    it.head = blk;
+  } else {
+    const int r = blk - D;
+    if (r < 2 * (H - D)) {
+      it.kind = (r & 1) ? 0 : 1;
+      it.head = (r & 1) ? D + (r >> 1) : (r >> 1);
+    } else {
+      it.kind = 1;
+      it.head = (H - D) + (r - 2 * (H - D));
+    }
+  }
+  return it;
+}
+
+constexpr int kSlots = 4;                          // TMEM item slots (128 columns each)
+
+template <int D, int N>
+struct TcLayout {
+  static constexpr int KB = D / 64;                 // 128-byte k-blocks per row
+  static constexpr int TI = 128 / N;                // tiles per item: one slot of 128 columns
+  static constexpr int A_BYTES = kTileKeys * 128;   // one k-block of a key tile
+  static constexpr int STAGE_BYTES = KB * A_BYTES;
+  static constexpr int QB_BYTES = N * 128;          // one k-block of the window queries
+  static constexpr int Q_BYTES = KB * QB_BYTES;
+  // Everything but the key-tile ring, then as many ring stages as the 227 KB of shared memory
+  // allow (at most 8): more bytes in flight per SM keep HBM busy at loaded-memory latency.
+  static constexpr int FIXED = 2 * Q_BYTES + 2 * 4 * N * 4 + 2 * N * 4 + 8 * (2 * 8 + 4 + 4 * 16 + 4 + 1) + 64 + 1024;
+  static constexpr int STAGES_FIT = (232448 - FIXED) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT < 8 ? STAGES_FIT : 8;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_Q = OFF_K + STAGES * STAGE_BYTES;
+  static constexpr int OFF_RED = OFF_Q + 2 * Q_BYTES;        // [2 groups][4 warps][N] floats
+  static constexpr int OFF_ROW = OFF_RED + 2 * 4 * N * 4;    // [2 groups][N] floats: per-row constants
+  static constexpr int OFF_BAR = OFF_ROW + 2 * N * 4;
+  static constexpr int NBAR = 2 * STAGES + 4 + kSlots * TI + kSlots + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  // + slack for 1024-byte alignment; at least 120 KB so that no two CTAs share an SM (each one
+  // allocates all 512 TMEM columns, and a second allocation on the same SM would block).
+  static constexpr int BYTES_USED = OFF_MISC + 64 + 1024;
+  static constexpr int BYTES = BYTES_USED > 120 * 1024 ? BYTES_USED : 120 * 1024;
+  static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, N);
+  static_assert(N % 16 == 0 && N >= 16 && N <= 64, "N");
+  static_assert(kSlots * TI * N == (int)kTmemCols, "four slots fill TMEM");
+  static_assert(QB_BYTES % 1024 == 0, "swizzle atoms");
+  static_assert(STAGES >= 2 && BYTES <= 232448, "shared memory");
+};
+
+struct Ctx {
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* q_full;
+  uint64_t* q_empty;
+  uint64_t* tile_full;
+  uint64_t* tmem_empty;
+  uint64_t* final_bar;
+  uint32_t* misc;   // [0] tmem base, [1] abort, [4] last CTA
+  volatile int* abort;
+};
+
+__device__ __forceinline__ void fail(const Ctx& c, int32_t* dev_status) {
+  report(dev_status, SNAPKV_ERR_TIMEOUT);
+  *c.abort = 1;
+}
+
+__device__ __forceinline__ int tiles_of(const TcArgs& a, int chunk, int TI) {
+  const int64_t key0 = (int64_t)chunk * a.keys_per_item;
+  const int64_t left = a.l_prompt - key0;
+  const int t = (int)((left + kTileKeys - 1) / kTileKeys);
+  return t < TI ? t : TI;
+}
+
+// Butterfly reduce-transpose of C per-lane values over the 32 lanes of a warp (max or sum):
+// afterwards lane l holds the warp-wide result of row l (C == 32) or of row l/2 (C == 16) in v[0].
+template <int C, int O>
+__device__ __forceinline__ void butterfly_max(float* v, int lane) {
+  if constexpr (O >= 1) {
+    if constexpr (C >= 2) {
+      constexpr int H = C / 2;
+      const bool upper = (lane & O) != 0;
+#pragma unroll
+      for (int k = 0; k < H; ++k) {
+        const float send = upper ? v[k] : v[k + H];
+        const float keep = upper ? v[k + H] : v[k];
+        v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, O));
+      }
+      butterfly_max<H, O / 2>(v, lane);
+    } else {
+      v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], O));
+      butterfly_max<1, O / 2>(v, lane);
+    }
+  }
+}
+
+template <int C, int O>
+__device__ __forceinline__ void butterfly_sum(float* v, int lane) {
+  if constexpr (O >= 1) {
+    if constexpr (C >= 2) {
+      constexpr int H = C / 2;
+      const bool upper = (lane & O) != 0;
+#pragma unroll
+      for (int k = 0; k < H; ++k) {
+        const float send = upper ? v[k] : v[k + H];
+        const float keep = upper ? v[k + H] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      butterfly_sum<H, O / 2>(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      butterfly_sum<1, O / 2>(v, lane);
+    }
+  }
+}
+
+template <int D, int N>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q, TcArgs a) {
+  using Lay = TcLayout<D, N>;
+  constexpr int TI = Lay::TI;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + Lay::OFF_BAR);
+  Ctx c;
+  c.full = bars;
+  c.empty = bars + Lay::STAGES;
+  c.q_full = bars + 2 * Lay::STAGES;
+  c.q_empty = c.q_full + 2;
+  c.tile_full = c.q_empty + 2;
+  c.tmem_empty = c.tile_full + kSlots * TI;
+  c.final_bar = c.tmem_empty + kSlots;
+  c.misc = reinterpret_cast<uint32_t*>(base + Lay::OFF_MISC);
+  c.abort = reinterpret_cast<volatile int*>(c.misc + 1);
+  float* red = reinterpret_cast<float*>(base + Lay::OFF_RED);
+  float* rowc = reinterpret_cast<float*>(base + Lay::OFF_ROW);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Lay::NBAR; ++i) ptx::mbar_init(bars + i, 1);
+    for (int i = 1; i < 8; ++i) c.misc[i] = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&c.misc[0], kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = c.misc[0];
+  __shared__ int no_abort;
+  if (threadIdx.x == 0) no_abort = 0;
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tmap_k);
+      ptx::prefetch_tensormap(&tmap_q);
+      const uint64_t keep = ptx::make_policy_evict_last();
+      const uint64_t drop = ptx::make_policy_evict_first();
+      uint32_t g = 0;
+      int n = 0;
+      for (;; ++n) {
+        const int p = blockIdx.x + n * gridDim.x;
+        if (p >= a.n_queue || *c.abort) break;
+        const Item it = queue_item(a, p);
+        const int qb = n & 1;
+        if (!ptx::mbar_wait(&c.q_empty[qb], ((n >> 1) & 1) ^ 1, c.abort, kWaitLimit)) {
+          fail(c, a.dev_status);
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(&c.q_full[qb], Lay::Q_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < Lay::KB; ++kb)
+          ptx::tma_load_3d(base + Lay::OFF_Q + qb * Lay::Q_BYTES + kb * Lay::QB_BYTES, &tmap_q, kb * 64, 0, it.head,
+                           &c.q_full[qb]);
+        const int tiles = tiles_of(a, it.chunk, TI);
+        const int key0 = it.chunk * a.keys_per_item;
+        const uint64_t policy = it.kind == 0 ? keep : drop;
+        bool ok = true;
+        for (int t = 0; t < tiles; ++t, ++g) {
+          const int stage = g % Lay::STAGES;
+          const uint32_t round = g / Lay::STAGES;
+          if (!ptx::mbar_wait(&c.empty[stage], (round & 1) ^ 1, c.abort, kWaitLimit)) {
+            fail(c, a.dev_status);
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&c.full[stage], Lay::STAGE_BYTES);
+#pragma unroll
+          for (int kb = 0; kb < Lay::KB; ++kb)
+            ptx::tma_load_3d_hint(base + Lay::OFF_K + stage * Lay::STAGE_BYTES + kb * Lay::A_BYTES, &tmap_k,
+                                  kb * 64, key0 + t * kTileKeys, it.head, &c.full[stage], policy);
+        }
+        if (!ok) {
+          ++n;
+          break;
+        }
+      }
+      // Drain: every copy this thread started must land before the CTA may exit.
+      const uint32_t issued = g;
+      for (uint32_t k = (issued > (uint32_t)Lay::STAGES ? issued - Lay::STAGES : 0u); k < issued; ++k)
+        ptx::mbar_wait(&c.full[k % Lay::STAGES], (k / Lay::STAGES) & 1, &no_abort, kDrainLimit);
+      for (int k = (n > 2 ? n - 2 : 0); k < n; ++k)
+        ptx::mbar_wait(&c.q_full[k & 1], (k >> 1) & 1, &no_abort, kDrainLimit);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t g = 0;
+      for (int n = 0;; ++n) {
+        const int p = blockIdx.x + n * gridDim.x;
+        if (p >= a.n_queue || *c.abort) break;
+        const Item it = queue_item(a, p);
+        const int slot = n % kSlots, use = n / kSlots, qb = n & 1;
+        if (!ptx::mbar_wait(&c.tmem_empty[slot], (use & 1) ^ 1, c.abort, kWaitLimit) ||
+            !ptx::mbar_wait(&c.q_full[qb], (n >> 1) & 1, c.abort, kWaitLimit)) {
+          fail(c, a.dev_status);
+          break;
+        }
+        ptx::tc_fence_after();
+        const int tiles = tiles_of(a, it.chunk, TI);
+        const uint32_t q_addr = ptx::smem_u32(base + Lay::OFF_Q + qb * Lay::Q_BYTES);
+        bool ok = true;
+        for (int t = 0; t < TI; ++t) {
+          if (t < tiles) {
+            const int stage = g % Lay::STAGES;
+            const uint32_t round = g / Lay::STAGES;
+            if (!ptx::mbar_wait(&c.full[stage], round & 1, c.abort, kWaitLimit)) {
+              fail(c, a.dev_status);
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t a_addr = ptx::smem_u32(base + Lay::OFF_K + stage * Lay::STAGE_BYTES);
+            const uint32_t d_tmem = tmem_base + (uint32_t)(slot * TI * N + t * N);
+#pragma unroll
+            for (int kb = 0; kb < Lay::KB; ++kb) {
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t ad = ptx::smem_desc_k_sw128(a_addr + kb * Lay::A_BYTES + ks * 32);
+                const uint64_t bd = ptx::smem_desc_k_sw128(q_addr + kb * Lay::QB_BYTES + ks * 32);
+                ptx::mma_bf16(d_tmem, ad, bd, Lay::IDESC, (kb | ks) != 0);
+              }
+            }
+            ptx::mma_commit(&c.empty[stage]);
+            ++g;
+          }
+          ptx::mma_commit(&c.tile_full[slot * TI + t]);
+        }
+        if (!ok) break;
+        ptx::mma_commit(&c.q_empty[qb]);
+      }
+      ptx::mma_commit(c.final_bar);
+      ptx::mbar_wait(c.final_bar, 0, &no_abort, kDrainLimit);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..9)
+    const int q4 = warp & 3;                         // TMEM lane quarter this warp may access
+    const int gw = (warp - 2) & 3;                   // warp within its group
+    const int grp = (warp - 2) >> 2;                 // group: items n = grp, grp + 2, ...
+    const int gtid = (threadIdx.x - 64) & 127;       // thread within its group
+    const int bar_id = 1 + grp;
+    const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+    const int key_in_tile = q4 * 32 + lane;
+    constexpr int R = N < 32 ? N : 32;               // rows per register chunk
+    float* gred = red + grp * 4 * N;
+    float* growc = rowc + grp * N;
+    __shared__ int sh_stop[2];
+
+    // Abort decision shared by the group's 128 threads (named barriers have no timeout, so every
+    // thread of a group must take the same path between them).
+    auto stop_uniform = [&]() -> bool {
+      if (gtid == 0) sh_stop[grp] = *c.abort;
+      ptx::named_barrier(bar_id, 128);
+      const bool r = sh_stop[grp] != 0;
+      ptx::named_barrier(bar_id, 128);
+      return r;
+    };
+    auto load_rows = [&](uint32_t col, float* acc) {
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < R; h += 16) ptx::tmem_ld16(tmem_base + lane_addr + col + h, acc + h);
+      ptx::tmem_wait_ld();
+    };
+    // Per-warp row results after a butterfly: lane l holds row l (R == 32) or l/2 (R == 16).
+    auto stash_rows = [&](float* v, int r0) {
+      if constexpr (R == 32) {
+        gred[gw * N + r0 + lane] = v[0];
+      } else {
+        if ((lane & 1) == 0) gred[gw * N + r0 + (lane >> 1)] = v[0];
+      }
+    };
+    // Waits (bounded) for the item's tiles in its TMEM slot. A timed-out wait only raises the abort
+    // flag: the thread carries on (reading stale TMEM is harmless) so that it meets its peers at
+    // every barrier.
+    auto wait_tiles = [&](int slot, int use) {
+      for (int t = 0; t < TI; ++t)
+        if (!ptx::mbar_wait(&c.tile_full[slot * TI + t], use & 1, c.abort, kWaitLimit)) fail(c, a.dev_status);
+      ptx::tc_fence_after();
+    };
+
+    // A item: per 32-row chunk, the row maxima, then the row sums of 2^(s - max). In re-read mode
+    // the slot is released after the last TMEM read.
+    auto item_stats = [&](int n, const Item& it) {
+      const int slot = n % kSlots;
+      const int tiles = tiles_of(a, it.chunk, TI);
+      const int64_t item_key0 = (int64_t)it.chunk * a.keys_per_item;
+      const int64_t lim = a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? a.l_prefix : a.l_prefix - 1;
+      wait_tiles(slot, n / kSlots);
+#pragma unroll 1
+      for (int r0 = 0; r0 < N; r0 += R) {
+        float v[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) v[i] = -INFINITY;
+        for (int t = 0; t < tiles; ++t) {
+          float acc[R];
+          load_rows((uint32_t)(slot * TI * N + t * N + r0), acc);
+          const int64_t tkey0 = item_key0 + t * kTileKeys;
+          if (tkey0 + kTileKeys <= a.l_prefix) {
+#pragma unroll
+            for (int i = 0; i < R; ++i) v[i] = fmaxf(v[i], acc[i]);
+          } else {
+            const int64_t key = tkey0 + key_in_tile;
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+              const int row = r0 + i;
+              const bool vis = row < a.l_obs && key < a.l_prompt &&
+                               (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + row : key <= lim);
+              if (vis) v[i] = fmaxf(v[i], acc[i]);
+            }
+          }
+        }
+        butterfly_max<R, 16>(v, lane);
+        stash_rows(v, r0);
+        ptx::named_barrier(bar_id, 128);
+        if (gtid < R) {
+          float mx = gred[r0 + gtid];
+#pragma unroll
+          for (int w = 1; w < 4; ++w) mx = fmaxf(mx, gred[w * N + r0 + gtid]);
+          growc[r0 + gtid] = mx * a.scale_log2;       // log2-domain row maximum (or -inf)
+        }
+        ptx::named_barrier(bar_id, 128);
+        float mrow[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) mrow[i] = growc[r0 + i];
+#pragma unroll
+        for (int i = 0; i < R; ++i) v[i] = 0.f;
+        for (int t = 0; t < tiles; ++t) {
+          float acc[R];
+          load_rows((uint32_t)(slot * TI * N + t * N + r0), acc);
+          const int64_t tkey0 = item_key0 + t * kTileKeys;
+          if (tkey0 + kTileKeys <= a.l_prefix) {
+#pragma unroll
+            for (int i = 0; i < R; ++i) v[i] += ex2(fmaf(acc[i], a.scale_log2, -mrow[i]));
+          } else {
+            const int64_t key = tkey0 + key_in_tile;
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+              const int row = r0 + i;
+              const bool vis = row < a.l_obs && key < a.l_prompt &&
+                               (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + row : key <= lim);
+              if (vis) v[i] += ex2(fmaf(acc[i], a.scale_log2, -mrow[i]));
+            }
+          }
+        }
+        const bool last_read = !a.resident && r0 + R >= N;   // resident items keep the slot
+        if (last_read) ptx::tc_fence_before();
+        butterfly_sum<R, 16>(v, lane);
+        stash_rows(v, r0);
+        ptx::named_barrier(bar_id, 128);
+        if (last_read && gtid == 0) ptx::mbar_arrive(&c.tmem_empty[slot]);
+        if (gtid < R && r0 + gtid < a.l_obs) {
+          float zz = gred[r0 + gtid];
+#pragma unroll
+          for (int w = 1; w < 4; ++w) zz += gred[w * N + r0 + gtid];
+          const float mx = growc[r0 + gtid];
+          if (zz > 0.f) {   // the row saw at least one visible key in this item
+            const float fl = floorf(mx);
+            if (fabsf(fl) > 1000.f) report(a.dev_status, SNAPKV_ERR_UNSUPPORTED);
+            // z * 2^M = (z * 2^(M - floor M)) * 2^floor M with z * 2^(M - floor M) in [1, 2^11):
+            // the fp64 bits are assembled from the fp32 bits (no fp64 arithmetic).
+            const uint32_t fb = __float_as_uint(zz * ex2(mx - fl));
+            const long long e = (long long)fminf(fmaxf(fl, -1000.f), 1000.f) + (long long)((fb >> 23) & 0xFF) - 127;
+            const long long db = ((e + 1023) << 52) | ((long long)(fb & 0x7FFFFF) << 29);
+            ptx::red_add_f64(a.zsum + (int64_t)it.head * a.l_obs + r0 + gtid, __longlong_as_double(db));
+          }
+        }
+        ptx::named_barrier(bar_id, 128);
+      }
+      // The group's reductions are ordered before the counter update by the barrier above; the
+      // release-ordered increment makes them visible to whoever acquires the counter.
+      if (gtid == 0) ptx::red_add_release_u32(a.cnt + it.head, 1u);
+    };
+
+    // B item (after its head's statistics are published): the vote of each prefix key,
+    // C_j = sum_i 2^(s'_ij - c_i); the slot is released after the last TMEM read.
+    auto item_vote = [&](int n, const Item& it) {
+      const int slot = n % kSlots;
+      const int tiles = tiles_of(a, it.chunk, TI);
+      const int64_t item_key0 = (int64_t)it.chunk * a.keys_per_item;
+      if (gtid == 0) {
+        const uint32_t need = (uint32_t)a.n_chunk;
+        if (ptx::ld_acquire_u32(a.cnt + it.head) < need) {
+          const long long t0 = clock64();
+          while (ptx::ld_acquire_u32(a.cnt + it.head) < need) {
+            if (*c.abort || clock64() - t0 > kWaitLimit) {
+              fail(c, a.dev_status);
+              break;
+            }
+            __nanosleep(32);
+          }
+        }
+      }
+      ptx::named_barrier(bar_id, 128);
+      if (gtid < N) {
+        float cv = INFINITY;   // rows past L_obs: zero logits, zero weight
+        if (gtid < a.l_obs) {
+          // log2 Z_i = exponent + log2(mantissa in [1, 2)), read off the fp64 bits
+          const long long zb = __double_as_longlong(__ldcg(a.zsum + (int64_t)it.head * a.l_obs + gtid));
+          const int e = (int)((zb >> 52) & 0x7FF) - 1023;
+          const float mant = __uint_as_float(0x3F800000u | (uint32_t)((zb >> 29) & 0x7FFFFF));
+          cv = (zb & 0x7FF0000000000000LL) ? (float)e + log2f(mant) : -INFINITY;
+        }
+        growc[gtid] = cv;
+      }
+      wait_tiles(slot, n / kSlots);
+      ptx::named_barrier(bar_id, 128);
+      float cr[N];
+#pragma unroll
+      for (int i = 0; i < N; ++i) cr[i] = growc[i];
+      for (int t = 0; t < tiles; ++t) {
+        const int64_t key = item_key0 + t * kTileKeys + key_in_tile;
+        float csum = 0.f;
+#pragma unroll
+        for (int r0 = 0; r0 < N; r0 += R) {
+          float acc[R];
+          load_rows((uint32_t)(slot * TI * N + t * N + r0), acc);
+#pragma unroll
+          for (int i = 0; i < R; ++i) csum += ex2(fmaf(acc[i], a.scale_log2, -cr[r0 + i]));
+        }
+        if (key < a.l_prefix) a.c_out[(int64_t)it.head * a.l_prefix + key] = csum;
+      }
+      ptx::tc_fence_before();
+      ptx::named_barrier(bar_id, 128);
+      if (gtid == 0) ptx::mbar_arrive(&c.tmem_empty[slot]);
+    };
+
+    // With at most grid items per head, the positions of a head's items are less than a grid apart,
+    // so no CTA holds two of them.
+    const bool lag0 = a.n_chunk <= (int)gridDim.x;
+    int k = 0;
+    for (;; ++k) {
+      const int n = grp + 2 * k;
+      const int p = blockIdx.x + n * gridDim.x;
+      if (p >= a.n_queue || stop_uniform()) break;
+      const Item it = queue_item(a, p);
+      if (it.kind == 0)
+        item_stats(n, it);
+      else
+        item_vote(n, it);
+      if (a.resident && lag0) {
+        // A head has at most one item on this CTA: its vote may wait for the head right away.
+        item_vote(n, it);
+      } else if (a.resident && k > 0) {
+        // Otherwise the vote of the group's previous item, whose logits are still in TMEM, comes
+        // after the statistics of this one (so no item of the CTA waits without its pass A).
+        const int m = n - 2;
+        item_vote(m, queue_item(a, blockIdx.x + m * gridDim.x));
+      }
+    }
+    if (a.resident && !lag0 && k > 0 && !stop_uniform()) {
+      const int m = grp + 2 * (k - 1);
+      item_vote(m, queue_item(a, blockIdx.x + m * gridDim.x));
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t old = atomicAdd(a.done, 1u);
+    c.misc[4] = (old == gridDim.x - 1) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (c.misc[4]) {
+    // Last CTA out: leave the per-head counters zeroed for the next call.
+    __threadfence();
+    for (int i = threadIdx.x; i < a.bh_total; i += kThreadsTc) a.cnt[i] = 0u;
+    for (int64_t i = threadIdx.x; i < (int64_t)a.bh_total * a.l_obs; i += kThreadsTc) a.zsum[i] = 0.0;
+    if (threadIdx.x == 0) *a.done = 0u;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* map, const void* ptr, int d, int64_t rows, int64_t heads, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int N>
+cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
+  using Lay = TcLayout<D, N>;
+  auto kern = vote_tc_kernel<D, N>;
+  if (grid <= 0) return cudaErrorInvalidConfiguration;   // tc_grid() also set the smem attribute
+  cudaError_t err;
+  CUtensorMap mk, mq;
+  const int64_t bh = (int64_t)job.batch * job.heads;
+  if (!make_map(&mk, job.k, D, job.l_prompt, bh, kTileKeys) || !make_map(&mq, job.q_obs, D, job.l_obs, bh, N))
+    return cudaErrorInvalidValue;
+  TcArgs a;
+  a.l_prompt = job.l_prompt;
+  a.l_prefix = job.l_prefix;
+  a.l_obs = job.l_obs;
+  a.scope = job.scope;
+  a.keys_per_item = Lay::TI * kTileKeys;
+  a.n_chunk = (int)((job.l_prompt + a.keys_per_item - 1) / a.keys_per_item);
+  a.bh_total = (int)bh;
+  a.resident = a.n_chunk <= kSlots * grid ? 1 : 0;
+  a.n_queue = (int)((a.resident ? 1 : 2) * bh * a.n_chunk);
+  // B items of a head come about four grids of queue positions after its last A item (so they
+  // seldom wait), unless the keys read in between would no longer fit comfortably in L2.
+  const int64_t want = 1 + (4 * (int64_t)grid + 2 * (int64_t)a.n_chunk - 1) / (2 * (int64_t)a.n_chunk);
+  const int64_t head_bytes = job.l_prompt * job.head_dim * 2;
+  const int64_t l2_fit = (int64_t)(64 << 20) / (head_bytes > 0 ? head_bytes : 1);
+  int64_t delta = want < l2_fit ? want : l2_fit;
+  if (delta < 1) delta = 1;
+  a.delta = (int)(delta < bh ? delta : bh);
+  a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)job.head_dim));
+  a.zsum = job.tc_zsum;
+  a.cnt = job.tc_cnt;
+  a.done = job.tc_done;
+  a.c_out = job.c;
+  a.dev_status = job.dev_status;
+  if (grid > a.n_queue) grid = a.n_queue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreadsTc);
+  cfg.dynamicSmemBytes = Lay::BYTES;
+  cfg.stream = job.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  job.mark(2 * kStageScore);
+  err = cudaLaunchKernelEx(&cfg, kern, mk, mq, a);
+  job.mark(2 * kStageScore + 1);
+  job.mark(2 * kStageVote);
+  job.mark(2 * kStageVote + 1);
+  return err;
+}
+
+// Grid of the persistent kernel on the current device: one CTA per SM (each owns all 512 TMEM
+// columns), or 0 if the kernel cannot be resident. The answer depends only on the device and the
+// instantiation, so it is looked up once per (device, instantiation) and cached; the kernel's
+// shared-memory attribute is set at the same time.
+template <int D, int N>
+int tc_grid() {
+  using Lay = TcLayout<D, N>;
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];   // 0: unknown, -1: not resident, > 0: grid
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  const int known = cache[dev].load(std::memory_order_acquire);
+  if (known != 0) return known > 0 ? known : 0;
+  int sms = 0, per_sm = 0;
+  int grid = -1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      cudaFuncSetAttribute(vote_tc_kernel<D, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES) ==
+          cudaSuccess &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vote_tc_kernel<D, N>, kThreadsTc, Lay::BYTES) ==
+          cudaSuccess &&
+      per_sm > 0)
+    grid = sms;
+  cache[dev].store(grid, std::memory_order_release);
+  return grid > 0 ? grid : 0;
+}
+
+template <int D>
+int tc_n_pad(int l_obs) {
+  return l_obs <= 16 ? 16 : (l_obs <= 32 ? 32 : 64);
+}
+
+}  // namespace
+
+int vote_tc_keys_per_item(int l_obs) { return (128 / tc_n_pad<128>(l_obs)) * kTileKeys; }
+
+bool vote_tc_eligible(const CompressJob& job) {
+  if (job.dtype != SNAPKV_BF16 || job.l_obs > 64) return false;
+  if (job.head_dim != 64 && job.head_dim != 128) return false;
+  const int n = tc_n_pad<128>(job.l_obs);
+  const int grid = job.head_dim == 64 ? (n == 16 ? tc_grid<64, 16>() : n == 32 ? tc_grid<64, 32>() : tc_grid<64, 64>())
+                                      : (n == 16 ? tc_grid<128, 16>() : n == 32 ? tc_grid<128, 32>() : tc_grid<128, 64>());
+  if (grid <= 0) return false;
+  const int64_t per_item = vote_tc_keys_per_item(job.l_obs);
+  const int64_t n_chunk = (job.l_prompt + per_item - 1) / per_item;
+  return 2 * n_chunk * job.batch * job.heads < ((int64_t)1 << 31);
+}
+
+cudaError_t launch_vote_tc(const CompressJob& job) {
+  const int n = tc_n_pad<128>(job.l_obs);
+  if (job.head_dim == 64) {
+    if (n == 16) return launch_tc_typed<64, 16>(job, tc_grid<64, 16>());
+    if (n == 32) return launch_tc_typed<64, 32>(job, tc_grid<64, 32>());
+    return launch_tc_typed<64, 64>(job, tc_grid<64, 64>());
+  }
+  if (n == 16) return launch_tc_typed<128, 16>(job, tc_grid<128, 16>());
+  if (n == 32) return launch_tc_typed<128, 32>(job, tc_grid<128, 32>());
+  return launch_tc_typed<128, 64>(job, tc_grid<128, 64>());
+}
+
+}  // namespace snapkv

@@ -23,6 +23,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT, ERR_W
     0, 1, 2, 4, 8, 16, 32, 64)
 F32, BF16 = 0, 1
 SCOPE_PROMPT_CAUSAL, SCOPE_PREFIX_ONLY = 0, 1
+ALGO_AUTO, ALGO_SIMT, ALGO_TENSOR_CORE = 0, 1, 2
+_ALGOS = {"auto": ALGO_AUTO, "simt": ALGO_SIMT, "tensor_core": ALGO_TENSOR_CORE}
 _SCOPES = {"prompt_causal": SCOPE_PROMPT_CAUSAL, "prefix_only": SCOPE_PREFIX_ONLY}
 
 
@@ -32,7 +34,7 @@ class CompressParams(ctypes.Structure):
         ("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
         ("l_obs", ctypes.c_int32), ("l_prompt", ctypes.c_int64), ("pool_kernel", ctypes.c_int32),
         ("softmax_scope", ctypes.c_int32), ("ratio_p", ctypes.c_double), ("budget", ctypes.c_int64),
-        ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("algo", ctypes.c_int32),
     ]
 
 
@@ -112,9 +114,9 @@ def _dtype_code(t) -> int:
 
 
 def make_params(*, batch, heads, head_dim, l_obs, l_prompt, pool_kernel, ratio_p=0.0, budget=0,
-                scope="prompt_causal", dtype=BF16) -> CompressParams:
+                scope="prompt_causal", dtype=BF16, algo="auto") -> CompressParams:
     return CompressParams(batch, heads, head_dim, l_obs, l_prompt, pool_kernel, _SCOPES[scope],
-                          float(ratio_p), int(budget), dtype, 0)
+                          float(ratio_p), int(budget), dtype, _ALGOS[algo])
 
 
 def kept(params: CompressParams) -> int:
@@ -135,7 +137,7 @@ def new_workspace(nbytes: int, device):
     return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
-def compress(q_obs, k, v, *, pool_kernel, ratio_p=0.0, budget=0, scope="prompt_causal", cap=None,
+def compress(q_obs, k, v, *, pool_kernel, ratio_p=0.0, budget=0, scope="prompt_causal", algo="auto", cap=None,
              k_out=None, v_out=None, len_out=None, idx_out=None, vote_out=None, want_idx=True,
              want_vote=False, workspace=None, dev_status=None, stream=None):
     """snapkv_compress on torch tensors q_obs [B,H,L_obs,d], k, v [B,H,L_prompt,d].
@@ -147,7 +149,7 @@ def compress(q_obs, k, v, *, pool_kernel, ratio_p=0.0, budget=0, scope="prompt_c
     B, H, L, d = k.shape
     l_obs = q_obs.shape[2]
     params = make_params(batch=B, heads=H, head_dim=d, l_obs=l_obs, l_prompt=L, pool_kernel=pool_kernel,
-                         ratio_p=ratio_p, budget=budget, scope=scope, dtype=_dtype_code(k))
+                         ratio_p=ratio_p, budget=budget, scope=scope, dtype=_dtype_code(k), algo=algo)
     ksel = kept(params)
     if ksel < 0:
         raise SnapKVError(ERR_INVALID_ARG, "snapkv_compress_kept")

@@ -24,14 +24,15 @@ def dev(gpu_device):
     return gpu_device
 
 
-def _run_workload(dev, wl, layer=0, seq0=0, nseq=None, l_prompt=None, heads=None, scope="prompt_causal"):
+def _run_workload(dev, wl, layer=0, seq0=0, nseq=None, l_prompt=None, heads=None, scope="prompt_causal",
+                  algo="auto"):
     from kv_cache_compression_gb300 import snapkv
     nseq = nseq if nseq is not None else wl.batch
     L = l_prompt if l_prompt is not None else wl.prompt_lengths()[seq0]
     q, k, v, _ = synth.device_inputs(wl, layer, seq0, nseq, L, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     res = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, ratio_p=wl.ratio_p, budget=wl.budget, scope=scope,
-                          want_vote=True, dev_status=status)
+                          algo=algo, want_vote=True, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     l_prefix = L - wl.l_obs
@@ -60,13 +61,19 @@ def test_tiny_fp32_prefix_only_scope(dev):
     _run_workload(dev, synth.WORKLOADS[0], scope="prefix_only")
 
 
-def test_llama_layer_every_head(dev):
-    _, excused = _run_workload(dev, synth.WORKLOADS[1])
-    print(f"boundary-excused indices: {excused}")
+@pytest.mark.parametrize("algo", ["tensor_core", "simt"])
+def test_llama_layer_every_head(dev, algo):
+    _, excused = _run_workload(dev, synth.WORKLOADS[1], algo=algo)
+    print(f"boundary-excused indices ({algo}): {excused}")
 
 
-def test_long_context_sampled_heads(dev):
-    _run_workload(dev, synth.WORKLOADS[3], heads=[0, 13, 31])
+@pytest.mark.parametrize("algo", ["tensor_core", "simt"])
+def test_long_context_sampled_heads(dev, algo):
+    _run_workload(dev, synth.WORKLOADS[3], heads=[0, 13, 31], algo=algo)
+
+
+def test_llama_layer_prefix_only_tensor_core(dev):
+    _run_workload(dev, synth.WORKLOADS[1].with_(heads=8), scope="prefix_only", algo="tensor_core")
 
 
 def test_prefill_32_layers_sampled(dev):
@@ -97,21 +104,32 @@ EDGE_CASES = [
 ]
 
 
+@pytest.mark.parametrize("algo", ["auto", "simt"])
 @pytest.mark.parametrize("case", EDGE_CASES, ids=lambda c: f"bf16={c[0]}-d{c[1]}-obs{c[2]}-K{c[3]}-L{c[4]}")
-def test_edge_cases(dev, case):
+def test_edge_cases(dev, case, algo):
     bf16, d, l_obs, pool, L, p, budget, scope, B, H = case
     wl = synth.Workload("edge", 40 + L % 17, bf16=bf16, batch=B, heads=H, head_dim=d, layers=1, l_prompt=L,
                         l_obs=l_obs, pool_kernel=pool, ratio_p=p, budget=budget)
-    _run_workload(dev, wl, scope=scope)
+    _run_workload(dev, wl, scope=scope, algo=algo)
 
 
-def test_zero_queries_keep_the_first_k(dev):
+def test_tensor_core_path_is_refused_when_ineligible(dev):
+    from kv_cache_compression_gb300 import snapkv
+    q = torch.zeros(1, 1, 32, 64, device=dev)
+    k = torch.zeros(1, 1, 256, 64, device=dev)
+    with pytest.raises(snapkv.SnapKVError) as e:
+        snapkv.compress(q, k, k.clone(), pool_kernel=7, budget=10, algo="tensor_core")   # fp32 input
+    assert e.value.status == snapkv.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("algo", ["tensor_core", "simt"])
+def test_zero_queries_keep_the_first_k(dev, algo):
     """q = 0 makes every pooled score equal; ties go to the lower index, so I = 0..k-1 exactly."""
     from kv_cache_compression_gb300 import snapkv
     B, H, L, lo, d = 1, 3, 3000, 32, 128
     k = torch.randn(B, H, L, d, generator=torch.Generator().manual_seed(0)).to(torch.bfloat16).to(dev)
     q = torch.zeros(B, H, lo, d, dtype=torch.bfloat16, device=dev)
-    res = snapkv.compress(q, k, k.clone(), pool_kernel=7, budget=300)
+    res = snapkv.compress(q, k, k.clone(), pool_kernel=7, budget=300, algo=algo)
     torch.cuda.synchronize()
     for h in range(H):
         assert res["idx"][0, h].cpu().tolist() == list(range(300))
@@ -124,8 +142,10 @@ def test_workspace_is_reusable(dev):
     first = snapkv.compress(q, k, v, pool_kernel=7, budget=wl.budget, want_vote=True)
     again = snapkv.compress(q, k, v, pool_kernel=7, budget=wl.budget, want_vote=True, workspace=first["workspace"])
     torch.cuda.synchronize()
+    # The tensor-core path sums each row's exponentials with fp64 atomics, whose order varies from
+    # run to run, so the vote may differ in its last bits; the selection and the copies do not.
+    assert torch.allclose(first["vote"], again["vote"], rtol=1e-6, atol=0)
     assert torch.equal(first["idx"], again["idx"])
-    assert torch.equal(first["vote"], again["vote"])
     assert torch.equal(first["k_out"], again["k_out"])
 
 

@@ -20,7 +20,8 @@ namespace snapkv {
 namespace {
 
 constexpr int kDecThreads = 128;
-constexpr int kSplitRows = 256;
+constexpr int kSplitRows = 128;
+constexpr int kMaxSplits = 512;   // <= the floats of sm_o in every instantiation
 
 __global__ void __launch_bounds__(256)
 append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, uint4* __restrict__ k_cache,
@@ -189,22 +190,46 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecArgs a) {
   __syncthreads();
   if (!sh_last) return;
   __threadfence();
+  // Last CTA of the head: merge the splits. The split maxima and sums are fetched in parallel
+  // into shared memory (reusing sm_o), then each output column sums its splits' weighted partial
+  // outputs with independent loads.
   const float* parts = a.partial + bh * a.n_split * (D + 2);
+  float* sw = &sm_o[0][0];                       // [n_split] weights, then the scalar total
+  float M = -INFINITY;
+  for (int sp = tid; sp < a.n_split; sp += kDecThreads) M = fmaxf(M, __ldcg(parts + sp * (D + 2) + D));
+  M = warp_max(M);
+  if (lane == 0) sm_m[warp] = M;
+  __syncthreads();
+  M = sm_m[0];
+#pragma unroll
+  for (int w = 1; w < kDecThreads / 32; ++w) M = fmaxf(M, sm_m[w]);
+  __syncthreads();
+  float lsum = 0.f;
+  for (int sp = tid; sp < a.n_split; sp += kDecThreads) {
+    const float ms = __ldcg(parts + sp * (D + 2) + D);
+    const float w = (ms == -INFINITY || M == -INFINITY) ? 0.f : ex2(ms - M);
+    sw[sp] = w;
+    lsum = fmaf(__ldcg(parts + sp * (D + 2) + D + 1), w, lsum);
+  }
+  lsum = warp_sum(lsum);
+  if (lane == 0) sm_l[warp] = lsum;
+  __syncthreads();
+  float ltot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kDecThreads / 32; ++w) ltot += sm_l[w];
   T* out = static_cast<T*>(a.out) + bh * D;
   for (int t = tid; t < D; t += kDecThreads) {
-    float M = -INFINITY;
-    for (int sp = 0; sp < a.n_split; ++sp) M = fmaxf(M, __ldcg(parts + sp * (D + 2) + D));
-    float ot = 0.f, lt = 0.f;
-    if (M != -INFINITY) {
-      for (int sp = 0; sp < a.n_split; ++sp) {
-        const float ms = __ldcg(parts + sp * (D + 2) + D);
-        if (ms == -INFINITY) continue;
-        const float w = ex2(ms - M);
-        ot = fmaf(__ldcg(parts + sp * (D + 2) + t), w, ot);
-        lt = fmaf(__ldcg(parts + sp * (D + 2) + D + 1), w, lt);
-      }
+    float ot = 0.f;
+    int sp = 0;
+    for (; sp + 4 <= a.n_split; sp += 4) {
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcg(parts + (sp + u) * (D + 2) + t);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) ot = fmaf(v[u], sw[sp + u], ot);
     }
-    store_out<T>(out + t, lt > 0.f ? ot / lt : 0.f);
+    for (; sp < a.n_split; ++sp) ot = fmaf(__ldcg(parts + sp * (D + 2) + t), sw[sp], ot);
+    store_out<T>(out + t, ltot > 0.f ? ot / ltot : 0.f);
   }
   if (tid == 0) a.tickets[bh] = 0u;
 }
@@ -220,8 +245,12 @@ cudaError_t launch_decode_typed(const DecodeJob& job, const DecArgs& a) {
 
 DecodeLayout decode_layout(int batch, int heads, int head_dim, int64_t cap) {
   DecodeLayout L;
-  L.split_rows = kSplitRows;
-  L.n_split = (int)((cap + kSplitRows - 1) / kSplitRows);
+  // 128-row splits, or longer ones (a multiple of 128) for caches beyond 512 splits: the merge
+  // keeps one weight per split in the CTA's shared memory.
+  int64_t rows = kSplitRows;
+  if ((cap + rows - 1) / rows > kMaxSplits) rows = ((cap + kMaxSplits - 1) / kMaxSplits + kSplitRows - 1) / kSplitRows * kSplitRows;
+  L.split_rows = (int)rows;
+  L.n_split = (int)((cap + rows - 1) / rows);
   if (L.n_split < 1) L.n_split = 1;
   const size_t bh = (size_t)batch * heads;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };

@@ -8,6 +8,13 @@
 // value. A three-digit MSB-first radix select (11 + 11 + 10 bits) finds tau, the k-th largest
 // pattern, and how many copies of tau to keep; one ordered compaction pass then keeps every
 // P_j > tau and the lowest-index copies of tau, writing the indices ascending.
+//
+// Two kernels: for prefixes up to kClusterMaxPrefix a cluster of up to 8 CTAs shares a head, each
+// CTA holding a contiguous slice of P in shared memory; the slices' histograms are summed through
+// distributed shared memory (each CTA owns a range of bins) and every CTA locates the same digit;
+// the compaction offsets of the slices are exchanged the same way. Longer prefixes take one CTA
+// per head with P in global memory.
+#include "sm100_ptx.cuh"
 #include "snapkv_common.cuh"
 #include "snapkv_internal.h"
 
@@ -17,6 +24,22 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxBins = 2048;
+
+// Histogram update aggregated over the warp: lanes holding the same digit add once, through
+// their lowest lane (the pooled votes share few leading bits, so plain atomics would pile onto a
+// handful of bins). Every lane of the warp must call it; `valid` masks lanes with nothing to add.
+__device__ __forceinline__ void warp_hist_add(uint32_t* hist, uint32_t digit, bool valid) {
+  const uint32_t active = __ballot_sync(0xffffffffu, valid);
+  if (!valid) return;
+  const uint32_t peers = __match_any_sync(active, digit);
+  if ((threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+}
+
+__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
 
 // Exclusive block-wide prefix sum of one value per thread (all threads must call).
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* sh_warp, uint32_t* total) {
@@ -72,15 +95,14 @@ pool_topk_kernel(const float* __restrict__ c_all, float* __restrict__ p_all, int
 
   // Radix select of the k-th largest bit pattern.
   uint32_t prefix = 0, mask = 0, krem = (uint32_t)k_sel;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
   for (int pass = 0; pass < 3; ++pass) {
-    const int shift = shifts[pass], nb = 1 << widths[pass];
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0), nb = pass < 2 ? 2048 : 1024;   // 11 + 11 + 10 bits
     for (int b = tid; b < nb; b += kThreads) hist[b] = 0u;
     __syncthreads();
-    for (int j = tid; j < L; j += kThreads) {
-      const uint32_t u = __float_as_uint(p[j]);
-      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & (uint32_t)(nb - 1)], 1u);
+    for (int j0 = 0; j0 < L; j0 += kThreads) {   // warp-uniform trip count
+      const int j = j0 + tid;
+      const uint32_t u = j < L ? __float_as_uint(p[j]) : 0u;
+      warp_hist_add(hist, (u >> shift) & (uint32_t)(nb - 1), j < L && (u & mask) == prefix);
     }
     __syncthreads();
     if (tid < 32) {
@@ -145,15 +167,217 @@ pool_topk_kernel(const float* __restrict__ c_all, float* __restrict__ p_all, int
   }
 }
 
+constexpr int kCThreads = 512;
+constexpr int kCWarps = kCThreads / 32;
+constexpr int kMaxCluster = 8;
+constexpr int64_t kClusterMaxSlice = 24 * 1024;   // vote elements per CTA held in shared memory (x2 with P)
+constexpr int64_t kClusterMaxPrefix = kMaxCluster * kClusterMaxSlice;
+
+// Exclusive prefix sum over the CTA (all threads must call).
+__device__ __forceinline__ uint32_t cta_exclusive_scan(uint32_t v, uint32_t* sh_warp) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < kCWarps ? sh_warp[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kCWarps) sh_warp[lane] = w;
+  }
+  __syncthreads();
+  const uint32_t out = (warp > 0 ? sh_warp[warp - 1] : 0u) + x - v;
+  __syncthreads();
+  return out;
+}
+
+// Shared-memory words of the cluster kernel: the pooled slice, then the vote with its halo during
+// the pool (this slice's histogram afterwards), then the two cluster-histogram buffers.
+constexpr int kHistWords = kMaxBins;
+constexpr int kSumWords = 2 * kMaxBins;
+
+__host__ __device__ constexpr int round4(int x) { return (x + 3) & ~3; }
+
+// One cluster per (sequence, head); CTA `rank` of the cluster owns P[rank * slice, ...).
+//
+// Each CTA keeps a copy of the cluster-wide histogram. In a radix pass every CTA histograms its
+// slice, then adds each non-empty bin into every CTA's copy with distributed-shared-memory
+// reductions; after one cluster barrier each CTA holds the whole histogram and finds the digit
+// locally. The copies alternate between two buffers, and a buffer is cleared right after its pass
+// so the pass after next can add into it.
+__global__ void __launch_bounds__(kCThreads)
+pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ idx_all, int64_t l_prefix,
+                         int radius, int64_t k_sel, int slice) {
+  extern __shared__ __align__(16) uint32_t sm[];
+  uint32_t* pbits = sm;                                      // [slice] pooled vote bit patterns
+  uint32_t* work = sm + round4(slice);                       // 16-B aligned
+  float* cbuf = reinterpret_cast<float*>(work);              // [slice + 2 * radius] vote with halo
+  uint32_t* hist = work;                                     // [kMaxBins] this slice's histogram
+  uint32_t* sums = work + round4(max(slice + 2 * radius, kHistWords));   // [2][kMaxBins] cluster histograms
+  uint32_t* sh_warp = sums + kSumWords;                      // [32]
+  uint32_t* counts = sh_warp + 32;                           // [8] packed (greater << 16 | equal) per slice
+  __shared__ uint32_t sh_digit, sh_above;
+
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint32_t rank = ptx::cluster_rank(), csize = ptx::cluster_size();
+  const int64_t bh = blockIdx.x / csize;
+  const float* c = c_all + bh * l_prefix;
+  int32_t* idx = idx_all + bh * k_sel;
+  const int L = (int)l_prefix;
+  const int j0 = min(L, (int)rank * slice), j1 = min(L, j0 + slice);
+  const int n = j1 - j0;
+
+  for (int b = tid; b < kSumWords; b += kCThreads) sums[b] = 0u;
+  ptx::cluster_arrive();   // this CTA's cluster histograms are clear (waited for before the first add)
+
+  // Max pool of the slice: the vote (L2-resident) with its halo is staged in shared memory by
+  // coalesced independent loads, -inf outside the prefix; then each P_j is a max over the window.
+  const int h0 = j0 - radius, hn = n + 2 * radius;
+  for (int q = tid; q < hn; q += kCThreads) {
+    const int j = h0 + q;
+    cbuf[q] = (j >= 0 && j < L) ? __ldcg(c + j) : -INFINITY;
+  }
+  __syncthreads();
+  for (int j = tid; j < n; j += kCThreads) {
+    float m = cbuf[j];
+    for (int q = 1; q <= 2 * radius; ++q) m = fmaxf(m, cbuf[j + q]);
+    pbits[j] = __float_as_uint(m);
+  }
+  __syncthreads();   // the histogram below reuses the staging buffer
+  uint32_t prefix = 0, mask = 0, krem = (uint32_t)k_sel;
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0), nb = pass < 2 ? 2048 : 1024;   // 11 + 11 + 10 bits
+    uint32_t* s = sums + (pass & 1) * kMaxBins;
+    for (int b = tid; b < nb; b += kCThreads) hist[b] = 0u;
+    __syncthreads();
+    for (int jb = 0; jb < n; jb += kCThreads) {   // warp-uniform trip count
+      const int j = jb + tid;
+      const uint32_t u = j < n ? pbits[j] : 0u;
+      warp_hist_add(hist, (u >> shift) & (uint32_t)(nb - 1), j < n && (u & mask) == prefix);
+    }
+    __syncthreads();
+    if (pass == 0) ptx::cluster_wait();
+    for (int b = tid; b < nb; b += kCThreads) {
+      const uint32_t v = hist[b];
+      if (v != 0u)
+        for (uint32_t r = 0; r < csize; ++r) ptx::dsmem_add_u32(ptx::map_rank(s + b, r), v);
+    }
+    ptx::cluster_sync();   // every slice's bins have been added into every copy
+
+    // Thread t holds the four bins of group t counted from the top; a block scan gives the values
+    // in higher groups, and the group where that count first reaches k resolves the digit.
+    const int ngroups = nb / 4;   // <= kCThreads
+    const int g = ngroups - 1 - tid;
+    uint4 g4 = make_uint4(0, 0, 0, 0);
+    if (tid < ngroups) g4 = *reinterpret_cast<const uint4*>(s + 4 * g);
+    const uint32_t cnt = g4.x + g4.y + g4.z + g4.w;
+    const uint32_t above = cta_exclusive_scan(cnt, sh_warp);
+    if (tid < ngroups && above < krem && krem <= above + cnt) {
+      uint32_t acc = above;
+      const uint32_t hb[4] = {g4.w, g4.z, g4.y, g4.x};   // bins 4g+3 .. 4g
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (acc + hb[q] >= krem) {
+          sh_digit = (uint32_t)(4 * g + 3 - q);
+          sh_above = acc;
+          break;
+        }
+        acc += hb[q];
+      }
+    }
+    __syncthreads();
+    prefix |= sh_digit << shift;
+    mask |= (uint32_t)(nb - 1) << shift;
+    krem -= sh_above;
+    if (pass == 0)   // cleared before this CTA arrives at the next pass's barrier
+      for (int b = tid; b < nb; b += kCThreads) s[b] = 0u;
+  }
+  const uint32_t tau = prefix, need_eq = krem;
+
+  // Ordered compaction: thread = contiguous run of the slice; slices in rank order. A slice holds
+  // fewer than 2^16 values, so its (greater, equal) counts scan as one packed word; each CTA
+  // stores its total into the later slices' CTAs.
+  const int per = (n + kCThreads - 1) / kCThreads;
+  const int a0 = min(n, tid * per), a1 = min(n, a0 + per);
+  uint32_t gt = 0, eq = 0;
+  for (int j = a0; j < a1; ++j) {
+    const uint32_t u = pbits[j];
+    gt += u > tau;
+    eq += u == tau;
+  }
+  const uint32_t packed = (gt << 16) | eq;
+  const uint32_t packed_in = cta_exclusive_scan(packed, sh_warp);
+  if (tid == kCThreads - 1)
+    for (uint32_t r = rank + 1; r < csize; ++r) ptx::dsmem_st_u32(ptx::map_rank(counts + rank, r), packed_in + packed);
+  ptx::cluster_sync();   // last access to another CTA's shared memory
+  const uint32_t before = (uint32_t)lane < rank ? counts[lane] : 0u;
+  const uint32_t gt_before = warp_sum_u32(before >> 16), eq_before = warp_sum_u32(before & 0xffffu);
+  // Output position of this run: every greater value before it, plus the equal values before it
+  // that are kept (the lowest-index need_eq copies of tau are kept).
+  const uint32_t e0 = eq_before + (packed_in & 0xffffu);
+  uint32_t pos = gt_before + (packed_in >> 16) + (e0 < need_eq ? e0 : need_eq);
+  uint32_t e = e0;
+  for (int j = a0; j < a1; ++j) {
+    const uint32_t u = pbits[j];
+    bool keep = u > tau;
+    if (u == tau) {
+      keep = e < need_eq;
+      ++e;
+    }
+    if (keep) {
+      if ((int64_t)pos < k_sel) idx[pos] = j0 + j;
+      ++pos;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_pool_topk(const CompressJob& job) {
   const int64_t bh = (int64_t)job.batch * job.heads;
   job.mark(2 * kStageTopk);
-  pool_topk_kernel<<<(unsigned)bh, kThreads, 0, job.stream>>>(job.c, job.p, job.idx, job.l_prefix,
-                                                              job.pool_kernel / 2, job.k_sel);
+  cudaError_t err = cudaSuccess;
+  if (job.k_sel <= 0) {
+    // Nothing is selected: no launch.
+  } else if (job.l_prefix <= kClusterMaxPrefix && job.pool_kernel <= 1025) {
+    int cl = (int)((job.l_prefix + 2047) / 2048);
+    if (cl > kMaxCluster) cl = kMaxCluster;
+    if (cl < 1) cl = 1;
+    const int slice = (int)((job.l_prefix + cl - 1) / cl);
+    const int work = slice + 2 * (job.pool_kernel / 2);
+    const size_t smem =
+        (size_t)(round4(slice) + round4(work > kHistWords ? work : kHistWords) + kSumWords + 32 + kMaxCluster) * sizeof(uint32_t);
+    err = cudaFuncSetAttribute(pool_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(bh * cl));
+    cfg.blockDim = dim3(kCThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = job.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, pool_topk_cluster_kernel, (const float*)job.c, job.idx, job.l_prefix,
+                             job.pool_kernel / 2, job.k_sel, slice);
+  } else {
+    pool_topk_kernel<<<(unsigned)bh, kThreads, 0, job.stream>>>(job.c, job.p, job.idx, job.l_prefix,
+                                                                job.pool_kernel / 2, job.k_sel);
+    err = cudaGetLastError();
+  }
   job.mark(2 * kStageTopk + 1);
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace snapkv

@@ -112,9 +112,9 @@ SNAPKV_API size_t snapkv_compress_workspace_size(const snapkv_compress_params* p
  * len_out   device int32 [B]             set to R for every sequence
  * idx_out   device int32 [B, H, k]       kept prefix positions, ascending (NULL: not returned)
  * vote_out  device fp32 [B, H, L_prefix] the vote C (NULL: not returned)
- * workspace device, >= snapkv_compress_workspace_size(params) bytes, 256-byte aligned; it must be
- *           zero-filled before its first use and is left zero-filled in its counter region on
- *           return, so one workspace can serve every later call (one call at a time)
+ * workspace device, >= snapkv_compress_workspace_size(params) bytes, 256-byte aligned: scratch
+ *           whose contents on entry do not matter (it needs no zero-fill, and one workspace can
+ *           serve calls of any shape that fits it, one call at a time on the GPU)
  * dev_status device int32 (optional)     error bits OR-ed in on the GPU
  */
 SNAPKV_API snapkv_status snapkv_compress(const snapkv_compress_params* params, const void* q_obs,
@@ -131,7 +131,9 @@ SNAPKV_API snapkv_status snapkv_compress(const snapkv_compress_params* params, c
  * window row), 1 vote, 2 max-pool + top-k, 3 gather + window append. Slots beyond n_events, or
  * NULL entries, are skipped; n_events = 0 behaves exactly like snapkv_compress. The events are
  * owned by the caller. A stage that needs no kernel for the given problem records its two
- * events back to back.
+ * events back to back. When `stream` is being captured into a CUDA graph, each record is
+ * captured as an event-record node (cudaEventRecordExternal), so every replay of the graph
+ * records the events again.
  */
 SNAPKV_API snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, const void* q_obs,
                                                   const void* k, const void* v, void* k_out, void* v_out,
@@ -168,8 +170,8 @@ SNAPKV_API size_t snapkv_decode_workspace_size(int32_t batch, int32_t heads, int
  * len               device int32 [B]; rows 0..len[b]-1 are attended. len[b] > cap is clamped to
  *                   cap and reported as SNAPKV_ERR_CAPACITY; len[b] <= 0 gives o = 0.
  * out               device [B, H, d], same dtype as the cache
- * workspace         device, >= snapkv_decode_workspace_size(...) bytes, 256-byte aligned,
- *                   zero-filled before first use (its counters are left zeroed on return)
+ * workspace         device, >= snapkv_decode_workspace_size(...) bytes, 256-byte aligned:
+ *                   scratch whose contents on entry do not matter (one call at a time on the GPU)
  */
 SNAPKV_API snapkv_status snapkv_decode_attend(const void* q, const void* k_cache, const void* v_cache,
                                    int64_t cap, const int32_t* len, void* out, int32_t batch,
@@ -187,8 +189,9 @@ SNAPKV_API snapkv_status snapkv_decode_attend(const void* q, const void* k_cache
  *
  * It allocates nothing. Its scratch (the split partials and the per-head tickets) is a 16 MiB
  * array built into the library, which every GPU that loads the library holds until the process
- * exits. A problem needing more than that — 256-byte-rounded B*H*ceil(cap/256)*(d+2)*4 bytes of
- * partials plus B*H*4 bytes of tickets — is rejected with SNAPKV_ERR_WORKSPACE before anything
+ * exits. A problem needing more than that — 256-byte-rounded B*H*S*(d+2)*4 bytes of partials,
+ * with S = ceil(cap/128) splits (longer splits once S would pass 512), plus B*H*4 bytes of
+ * tickets — is rejected with SNAPKV_ERR_WORKSPACE before anything
  * is enqueued. The first call on a device looks up the array's device address (once per device,
  * with that device current), so make that first call before any stream capture. Every call
  * shares the one array and it keeps the last call's contents (the tickets are cleared on `stream`

@@ -70,7 +70,7 @@ CompressLayout compress_layout(int batch, int heads, int l_obs, int64_t l_prompt
   L.idx = L.p + up256(bh * l_prefix * sizeof(float));
   L.tc_zsum = L.idx + up256(bh * (k_sel > 0 ? k_sel : 1) * sizeof(int32_t));
   L.tc_counters = L.tc_zsum + up256(bh * l_obs * sizeof(double));
-  L.total = L.tc_counters + up256((bh + 1) * sizeof(uint32_t));
+  L.total = L.tc_counters + up256(bh * sizeof(uint32_t));
   return L;
 }
 
@@ -170,7 +170,7 @@ snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, con
   job.partial = reinterpret_cast<float*>(ws + L.partial);
   job.tc_zsum = reinterpret_cast<double*>(ws + L.tc_zsum);
   job.tc_cnt = reinterpret_cast<uint32_t*>(ws + L.tc_counters);
-  job.tc_done = job.tc_cnt + bh;
+  job.tc_zero_bytes = L.total - L.tc_zsum;
   job.vote_chunk = L.vote_chunk;
   job.n_chunk_all = L.n_chunk_all;
   job.n_chunk_prefix = L.n_chunk_prefix;

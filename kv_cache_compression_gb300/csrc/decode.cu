@@ -231,7 +231,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecArgs a) {
     for (; sp < a.n_split; ++sp) ot = fmaf(__ldcg(parts + sp * (D + 2) + t), sw[sp], ot);
     store_out<T>(out + t, ltot > 0.f ? ot / ltot : 0.f);
   }
-  if (tid == 0) a.tickets[bh] = 0u;
 }
 
 template <typename T, int D>
@@ -306,9 +305,6 @@ cudaError_t launch_decode_noalloc(DecodeJob job) {
   job.tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
   job.split_rows = L.split_rows;
   job.n_split = L.n_split;
-  // The array keeps whatever the last call left; the tickets must start at zero.
-  err = cudaMemsetAsync(job.tickets, 0, (size_t)job.batch * job.heads * sizeof(uint32_t), job.stream);
-  if (err != cudaSuccess) return err;
   return launch_decode(job);
 }
 
@@ -327,6 +323,10 @@ cudaError_t launch_decode(const DecodeJob& job) {
   a.n_split = job.n_split;
   a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)job.head_dim));
   a.dev_status = job.dev_status;
+  // The per-head tickets start at zero on every call (the workspace's contents are not trusted).
+  const cudaError_t err =
+      cudaMemsetAsync(job.tickets, 0, (size_t)job.batch * job.heads * sizeof(uint32_t), job.stream);
+  if (err != cudaSuccess) return err;
   if (job.dtype == SNAPKV_BF16)
     return job.head_dim == 64 ? launch_decode_typed<__nv_bfloat16, 64>(job, a)
                               : launch_decode_typed<__nv_bfloat16, 128>(job, a);

@@ -182,36 +182,6 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Atomic add with acquire-release semantics at GPU scope: releases every write that happens before
-// it (including other threads' writes ordered before it by a barrier) and acquires the writes
-// released by earlier atomics on the same counter.
-__device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-// Fire-and-forget reductions (no value returned, so nothing waits on the round trip).
-__device__ __forceinline__ void red_add_f64(double* p, double v) {
-  asm volatile("red.global.add.f64 [%0], %1;" ::"l"(p), "d"(v) : "memory");
-}
-
-// Release-ordered increment: every write that happens before it (including other threads' writes
-// and reductions ordered before it by a barrier) is visible to a thread that acquires the counter.
-__device__ __forceinline__ void red_add_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // ---------------------------------------------------------------- clusters / distributed shared memory
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -228,6 +198,23 @@ __device__ __forceinline__ uint32_t cluster_size() {
 // All threads of all CTAs of the cluster; orders shared-memory (including remote) accesses.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Fire-and-forget reduction (no value returned, so nothing waits on the round trip).
+__device__ __forceinline__ void red_add_f64(double* p, double v) {
+  asm volatile("red.global.add.f64 [%0], %1;" ::"l"(p), "d"(v) : "memory");
+}
+
+// Release-ordered increment: every write that happens before it (including other threads' writes
+// and reductions ordered before it by a barrier) is visible to a thread that acquires the counter.
+__device__ __forceinline__ void red_add_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // The two halves of cluster_sync, for work that can run between them.

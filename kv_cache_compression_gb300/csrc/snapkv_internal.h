@@ -21,9 +21,9 @@ struct CompressJob {
   float* c;            // vote (caller's buffer or workspace)
   float* p;            // pooled vote (workspace)
   float* partial;      // per-chunk row statistics (workspace)
-  double* tc_zsum;     // per-(head, row) fp64 sums of 2^(logit) (workspace, zero between calls)
-  uint32_t* tc_cnt;    // per-head statistics items done (workspace, zero between calls)
-  uint32_t* tc_done;   // CTAs finished (workspace, zero between calls)
+  double* tc_zsum;     // per-(head, row) fp64 sums of 2^(logit) (workspace; zeroed per call)
+  uint32_t* tc_cnt;    // per-head statistics items done (workspace, right after tc_zsum)
+  size_t tc_zero_bytes;   // bytes from tc_zsum through the counters, cleared before the kernel
   int vote_chunk;      // keys per chunk of the score/vote kernels
   int n_chunk_all;     // chunks covering the whole prompt
   int n_chunk_prefix;  // chunks covering the prefix
@@ -31,8 +31,15 @@ struct CompressJob {
   cudaStream_t stream;
   cudaEvent_t* events;  // optional stage events (see snapkv_compress_profiled), may be null
   int n_events;
+  // Records stage event `slot`. Inside a stream capture the record becomes an event-record node of
+  // the graph (an external event), so that replays of the graph time the stage too.
   void mark(int slot) const {
-    if (events && slot < n_events && events[slot]) cudaEventRecord(events[slot], stream);
+    if (!events || slot >= n_events || !events[slot]) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+      cudaEventRecordWithFlags(events[slot], stream, cudaEventRecordExternal);
+    else
+      cudaEventRecord(events[slot], stream);
   }
 };
 

@@ -61,7 +61,6 @@ struct TcArgs {
   float scale_log2;
   double* zsum;      // [BH][l_obs]: Z_i = sum_j 2^(s'_ij) over the head's visible keys (fp64)
   uint32_t* cnt;     // [BH] A items whose contribution to zsum is complete
-  uint32_t* done;    // [1] CTAs finished
   float* c_out;      // [BH][l_prefix]
   int32_t* dev_status;
 };
@@ -141,7 +140,7 @@ struct Ctx {
   uint64_t* tile_full;
   uint64_t* tmem_empty;
   uint64_t* final_bar;
-  uint32_t* misc;   // [0] tmem base, [1] abort, [4] last CTA
+  uint32_t* misc;   // [0] tmem base, [1] abort
   volatile int* abort;
 };
 
@@ -567,19 +566,6 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const uint32_t old = atomicAdd(a.done, 1u);
-    c.misc[4] = (old == gridDim.x - 1) ? 1u : 0u;
-  }
-  __syncthreads();
-  if (c.misc[4]) {
-    // Last CTA out: leave the per-head counters zeroed for the next call.
-    __threadfence();
-    for (int i = threadIdx.x; i < a.bh_total; i += kThreadsTc) a.cnt[i] = 0u;
-    for (int64_t i = threadIdx.x; i < (int64_t)a.bh_total * a.l_obs; i += kThreadsTc) a.zsum[i] = 0.0;
-    if (threadIdx.x == 0) *a.done = 0u;
-  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -638,7 +624,6 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)job.head_dim));
   a.zsum = job.tc_zsum;
   a.cnt = job.tc_cnt;
-  a.done = job.tc_done;
   a.c_out = job.c;
   a.dev_status = job.dev_status;
   if (grid > a.n_queue) grid = a.n_queue;
@@ -653,6 +638,9 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   job.mark(2 * kStageScore);
+  // The row sums and per-head counters start at zero on every call (the workspace is scratch).
+  err = cudaMemsetAsync(job.tc_zsum, 0, job.tc_zero_bytes, job.stream);
+  if (err != cudaSuccess) return err;
   err = cudaLaunchKernelEx(&cfg, kern, mk, mq, a);
   job.mark(2 * kStageScore + 1);
   job.mark(2 * kStageVote);

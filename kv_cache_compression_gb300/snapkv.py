@@ -132,9 +132,9 @@ def decode_workspace_size(batch, heads, head_dim, cap) -> int:
 
 
 def new_workspace(nbytes: int, device):
-    """A zero-filled workspace (the library leaves its counters zeroed for the next call)."""
+    """A workspace buffer (scratch: the library needs no particular contents on entry)."""
     import torch
-    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
 def compress(q_obs, k, v, *, pool_kernel, ratio_p=0.0, budget=0, scope="prompt_causal", algo="auto", cap=None,

@@ -149,6 +149,40 @@ def test_workspace_is_reusable(dev):
     assert torch.equal(first["k_out"], again["k_out"])
 
 
+@pytest.mark.parametrize("algo", ["auto", "simt"])
+def test_garbage_workspace_shared_across_shapes(dev, algo):
+    """The workspace is scratch: random contents, and reuse by a call of another shape, change nothing."""
+    from kv_cache_compression_gb300 import snapkv
+    shapes = [(synth.WORKLOADS[1].with_(heads=2, l_prompt=3000), 7), (synth.WORKLOADS[1].with_(heads=5, l_prompt=9000), 5),
+              (synth.WORKLOADS[1].with_(heads=3, l_prompt=1500, l_obs=16), 9)]
+    need = max(snapkv.compress_workspace_size(snapkv.make_params(batch=1, heads=wl.heads, head_dim=wl.head_dim,
+                                                                  l_obs=wl.l_obs, l_prompt=wl.l_prompt,
+                                                                  pool_kernel=pk, budget=wl.budget,
+                                                                  dtype=snapkv.BF16))
+               for wl, pk in shapes)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, generator=torch.Generator().manual_seed(3)).to(dev)
+    for round_ in range(2):
+        for wl, pk in shapes:
+            q, k, v, _ = synth.device_inputs(wl, round_, 0, 1, wl.l_prompt, dev)
+            fresh = snapkv.compress(q, k, v, pool_kernel=pk, budget=wl.budget, algo=algo, want_vote=True)
+            shared = snapkv.compress(q, k, v, pool_kernel=pk, budget=wl.budget, algo=algo, want_vote=True, workspace=ws)
+            torch.cuda.synchronize()
+            if algo == "simt":   # fixed summation order: bit for bit
+                assert torch.equal(fresh["vote"], shared["vote"])
+                assert torch.equal(fresh["idx"], shared["idx"])
+                assert torch.equal(fresh["k_out"], shared["k_out"]) and torch.equal(fresh["v_out"], shared["v_out"])
+            else:                # fp64 atomics in a varying order: the last bits of the vote may differ
+                assert torch.allclose(fresh["vote"], shared["vote"], rtol=1e-6, atol=0)
+            for h in range(wl.heads):
+                hi = synth.host_head(wl, round_, 0, h, l_prompt=wl.l_prompt)
+                ref = orc.compress_head(hi.q_obs, hi.k, hi.v, pool_kernel=pk, budget=wl.budget)
+                check_compress_head(gpu_idx=shared["idx"][0, h].cpu().numpy(),
+                                    gpu_kc=to_numpy_f32(shared["k_out"][0, h]),
+                                    gpu_vc=to_numpy_f32(shared["v_out"][0, h]),
+                                    gpu_vote=shared["vote"][0, h].cpu().numpy(), ref=ref, k_in=hi.k, v_in=hi.v,
+                                    l_prefix=wl.l_prompt - wl.l_obs, l_obs=wl.l_obs, where=f"shape {wl.l_prompt} head {h}")
+
+
 def test_device_generator_matches_host(dev):
     wl = synth.WORKLOADS[2]
     q, k, v, _ = synth.device_inputs(wl, 5, 3, 1, 2048, dev)

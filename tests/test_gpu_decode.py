@@ -132,3 +132,21 @@ def test_compressed_decode_workload_sampled(dev):
                 kc, vc = orc.append(kc, vc, kn, vn)
                 check_decode(to_numpy_f32(outs[t][j]), orc.decode_attend(qn, kc, vc), True,
                              where=f"seq {seq} layer {layer} head {h} step {t}")
+
+
+def test_decode_garbage_workspace_shared_across_shapes(dev):
+    """The decode workspace is scratch: random contents and reuse by another shape change nothing."""
+    from kv_cache_compression_gb300 import snapkv
+    g = torch.Generator().manual_seed(11)
+    shapes = [(2, 3, 300), (6, 4, 1500), (1, 2, 90)]
+    need = max(snapkv.decode_workspace_size(B, H, 128, cap) for B, H, cap in shapes)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, generator=g).to(dev)
+    for B, H, cap in shapes * 2:
+        kc = torch.randn(B, H, cap, 128, generator=g).to(torch.bfloat16).to(dev)
+        vc = torch.randn(B, H, cap, 128, generator=g).to(torch.bfloat16).to(dev)
+        q = torch.randn(B, H, 128, generator=g).to(torch.bfloat16).to(dev)
+        length = torch.randint(1, cap + 1, (B,), generator=g, dtype=torch.int32).to(dev)
+        fresh = snapkv.decode_attend(q, kc, vc, length)
+        shared = snapkv.decode_attend(q, kc, vc, length, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(fresh, shared)

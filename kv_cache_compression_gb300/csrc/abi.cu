@@ -191,8 +191,14 @@ snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, con
     }
   }
   if (!voted && launch_vote_simt(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
-  if (launch_pool_topk(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
-  if (launch_gather(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  bool gathered = false;
+  if (launch_pool_topk(job, &gathered) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  if (gathered) {   // the gather stage ran inside the top-k kernel
+    job.mark(2 * kStageGather);
+    job.mark(2 * kStageGather + 1);
+  } else if (launch_gather(job) != cudaSuccess) {
+    return SNAPKV_ERR_CUDA;
+  }
   return SNAPKV_OK;
 }
 

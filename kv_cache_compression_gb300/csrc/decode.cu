@@ -2,12 +2,18 @@
 //
 // KV-cache chapter ("第22章 KV Cache"), section 22.2: K_cache <- [K_cache; k_t],
 // V_cache <- [V_cache; v_t], then o_t = softmax(q_t K_cache^T / sqrt(d_h)) V_cache with every cached
-// row visible. Each (sequence, head) cache is cut into splits of `split_rows` rows; one CTA per
-// split keeps an online softmax (running max m, running sum l, unnormalised output o) in the log2
-// domain, writes (m, l, o) to the workspace, and the last CTA of the head to finish (an atomic
-// ticket, no waiting) merges the splits and writes o / l.
+// row visible. Each CTA keeps an online softmax (running max m, running sum l, unnormalised output
+// o) in the log2 domain over its share of a head's rows. Two kernels:
+//   * caches of up to kClusterMaxCap rows: one thread-block cluster (up to 8 CTAs) per (sequence,
+//     head); the CTAs split the head's cap rows evenly (so the row loads need not wait for len; rows
+//     at or past len are masked), and after one cluster barrier each CTA
+//     finishes a slice of the output columns from every CTA's (m, l, o) read through distributed
+//     shared memory. No workspace is touched.
+//   * longer caches: splits of `split_rows` rows, one CTA each, partials in the workspace, and the
+//     last CTA of the head to finish (an atomic ticket, no waiting) merges them.
 #include <mutex>
 
+#include "sm100_ptx.cuh"
 #include "snapkv_common.cuh"
 #include "snapkv_internal.h"
 
@@ -22,6 +28,9 @@ namespace {
 constexpr int kDecThreads = 128;
 constexpr int kSplitRows = 128;
 constexpr int kMaxSplits = 512;   // <= the floats of sm_o in every instantiation
+constexpr int kClThreads = 256;
+constexpr int kClMaxCtas = 8;
+constexpr int64_t kClusterMaxCap = 16384;
 
 __global__ void __launch_bounds__(256)
 append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, uint4* __restrict__ k_cache,
@@ -233,6 +242,172 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecArgs a) {
   }
 }
 
+// One cluster per (sequence, head): CTA `rank` takes rows [rank * per, (rank + 1) * per) of the
+// head's cap rows (those at or past len masked), with up to UNROLL rows per lane group in flight.
+template <typename T, int D>
+__global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(DecArgs a) {
+  constexpr int V = Elem<T>::kVec;
+  constexpr int LPR = D / V;                       // lanes per cache row
+  constexpr int RPW = 32 / LPR;                    // rows per warp step
+  constexpr int GROUPS = (kClThreads / 32) * RPW;  // row groups per CTA
+  constexpr int UNROLL = 8;
+  __shared__ float sm_m[GROUPS], sm_l[GROUPS];
+  __shared__ __align__(16) float sm_o[GROUPS][D];
+  __shared__ float cta_m, cta_l;                   // this CTA's partial, read by the whole cluster
+  __shared__ __align__(16) float cta_o[D];
+
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  const uint32_t rank = ptx::cluster_rank(), csize = ptx::cluster_size();
+  const int64_t bh = blockIdx.x / csize;
+  const int b = (int)(bh / a.heads);
+  int n = a.len[b];
+  if ((int64_t)n > a.cap) {
+    if (rank == 0 && tid == 0 && bh % a.heads == 0) report(a.dev_status, SNAPKV_ERR_CAPACITY);
+    n = (int)a.cap;
+  }
+  if (n < 0) n = 0;
+  const int cap = (int)a.cap;
+  const int per = (cap + (int)csize - 1) / (int)csize;
+  const int r0 = min(cap, (int)rank * per);
+  const int r1 = min(cap, r0 + per);   // rows at or past n are loaded (they are inside cap) and masked
+  const int sub = lane / LPR, cl = lane % LPR;
+  const int group = warp * RPW + sub;
+
+  const T* qp = static_cast<const T*>(a.q) + bh * D;
+  float q[V];
+  Elem<T>::widen(ld_nc_v4(qp + cl * V), q);
+#pragma unroll
+  for (int e = 0; e < V; ++e) q[e] *= a.scale_log2;
+
+  const T* kc = static_cast<const T*>(a.k_cache) + bh * a.cap * D + cl * V;
+  const T* vc = static_cast<const T*>(a.v_cache) + bh * a.cap * D + cl * V;
+  float m = -INFINITY, l = 0.f, o[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) o[e] = 0.f;
+
+  // The trip count depends only on the CTA's range, so every lane of a warp runs the same
+  // iterations (the row reductions below shuffle across the whole warp).
+  for (int base = r0; base < r1; base += GROUPS * UNROLL) {
+    const int rb = base + group;
+    uint4 kr[UNROLL], vr[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int r = rb + u * GROUPS;
+      if (r < r1) {
+        kr[u] = ld_stream_v4(kc + (int64_t)r * D);
+        vr[u] = ld_stream_v4(vc + (int64_t)r * D);
+      } else {
+        kr[u] = make_uint4(0, 0, 0, 0);
+        vr[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    float s[UNROLL];
+    float smax = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      float kf[V];
+      Elem<T>::widen(kr[u], kf);
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < V; ++e) dot = fmaf(q[e], kf[e], dot);
+#pragma unroll
+      for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      const int r = rb + u * GROUPS;
+      s[u] = (r < r1 && r < n) ? dot : -INFINITY;
+      smax = fmaxf(smax, s[u]);
+    }
+    const float m_new = fmaxf(m, smax);
+    if (m_new == -INFINITY) continue;
+    const float corr = ex2(m - m_new);
+    l *= corr;
+#pragma unroll
+    for (int e = 0; e < V; ++e) o[e] *= corr;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const float p = ex2(s[u] - m_new);   // 0 for masked rows
+      float vf[V];
+      Elem<T>::widen(vr[u], vf);
+      l += p;
+#pragma unroll
+      for (int e = 0; e < V; ++e) o[e] = fmaf(p, vf[e], o[e]);
+    }
+    m = m_new;
+  }
+
+  if (cl == 0) {
+    sm_m[group] = m;
+    sm_l[group] = l;
+  }
+#pragma unroll
+  for (int e = 0; e < V; ++e) sm_o[group][cl * V + e] = o[e];
+  __syncthreads();
+  // This CTA's partial: column t combines the row groups.
+  if (tid < D) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < GROUPS; ++g) M = fmaxf(M, sm_m[g]);
+    float ot = 0.f, lt = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int g = 0; g < GROUPS; ++g) {
+        if (sm_m[g] == -INFINITY) continue;
+        const float w = ex2(sm_m[g] - M);
+        ot = fmaf(sm_o[g][tid], w, ot);
+        lt = fmaf(sm_l[g], w, lt);
+      }
+    }
+    cta_o[tid] = ot;
+    if (tid == 0) {
+      cta_m = M;
+      cta_l = lt;
+    }
+  }
+  ptx::cluster_sync();   // every CTA's partial is complete
+  // Column t is finished by CTA t % csize from all the cluster's partials.
+  T* out = static_cast<T*>(a.out) + bh * D;
+  for (int t = (int)rank + (int)csize * tid; t < D; t += (int)csize * kClThreads) {
+    float mr[kClMaxCtas];
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kClMaxCtas; ++r) {
+      mr[r] = r < (int)csize ? __uint_as_float(ptx::dsmem_ld_u32(ptx::map_rank(&cta_m, (uint32_t)r))) : -INFINITY;
+      M = fmaxf(M, mr[r]);
+    }
+    float lt = 0.f, ot = 0.f;
+#pragma unroll
+    for (int r = 0; r < kClMaxCtas; ++r) {
+      if (r < (int)csize && mr[r] != -INFINITY) {
+        const float w = ex2(mr[r] - M);
+        lt = fmaf(__uint_as_float(ptx::dsmem_ld_u32(ptx::map_rank(&cta_l, (uint32_t)r))), w, lt);
+        ot = fmaf(__uint_as_float(ptx::dsmem_ld_u32(ptx::map_rank(&cta_o[t], (uint32_t)r))), w, ot);
+      }
+    }
+    store_out<T>(out + t, lt > 0.f ? ot / lt : 0.f);
+  }
+  ptx::cluster_sync();   // no CTA leaves while its partial may still be read
+}
+
+template <typename T, int D>
+cudaError_t launch_decode_cluster(const DecodeJob& job, const DecArgs& a) {
+  const int64_t bh = (int64_t)job.batch * job.heads;
+  int csize = (int)((job.cap + kSplitRows - 1) / kSplitRows);
+  if (csize > kClMaxCtas) csize = kClMaxCtas;
+  if (csize < 1) csize = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(bh * csize));
+  cfg.blockDim = dim3(kClThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = job.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_cluster_kernel<T, D>, a);
+}
+
 template <typename T, int D>
 cudaError_t launch_decode_typed(const DecodeJob& job, const DecArgs& a) {
   const int64_t bh = (int64_t)job.batch * job.heads;
@@ -323,6 +498,12 @@ cudaError_t launch_decode(const DecodeJob& job) {
   a.n_split = job.n_split;
   a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)job.head_dim));
   a.dev_status = job.dev_status;
+  if (job.cap <= kClusterMaxCap) {
+    if (job.dtype == SNAPKV_BF16)
+      return job.head_dim == 64 ? launch_decode_cluster<__nv_bfloat16, 64>(job, a)
+                                : launch_decode_cluster<__nv_bfloat16, 128>(job, a);
+    return job.head_dim == 64 ? launch_decode_cluster<float, 64>(job, a) : launch_decode_cluster<float, 128>(job, a);
+  }
   // The per-head tickets start at zero on every call (the workspace's contents are not trusted).
   const cudaError_t err =
       cudaMemsetAsync(job.tickets, 0, (size_t)job.batch * job.heads * sizeof(uint32_t), job.stream);

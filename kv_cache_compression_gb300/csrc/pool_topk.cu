@@ -11,9 +11,11 @@
 //
 // Two kernels: for prefixes up to kClusterMaxPrefix a cluster of up to 8 CTAs shares a head, each
 // CTA holding a contiguous slice of P in shared memory; the slices' histograms are summed through
-// distributed shared memory (each CTA owns a range of bins) and every CTA locates the same digit;
-// the compaction offsets of the slices are exchanged the same way. Longer prefixes take one CTA
-// per head with P in global memory.
+// distributed shared memory and every CTA locates the same digit; the compaction offsets of the
+// slices are exchanged the same way. That kernel also does the gather of the section アルゴリズム
+// (K_c = [K[I]; K[L_prefix:]], V_c likewise): a CTA's kept indices are a contiguous block of the
+// ascending output, so it copies its own kept rows, and a share of the window rows. Longer
+// prefixes take one CTA per head with P in global memory, followed by the separate gather kernel.
 #include "sm100_ptx.cuh"
 #include "snapkv_common.cuh"
 #include "snapkv_internal.h"
@@ -213,9 +215,20 @@ __host__ __device__ constexpr int round4(int x) { return (x + 3) & ~3; }
 // reductions; after one cluster barrier each CTA holds the whole histogram and finds the digit
 // locally. The copies alternate between two buffers, and a buffer is cleared right after its pass
 // so the pass after next can add into it.
+// Row copies of the fused gather: K and V rows of `vpr` 16-byte pieces.
+struct GatherArgs {
+  const uint4* k;
+  const uint4* v;
+  uint4* k_out;
+  uint4* v_out;
+  int32_t* len_out;
+  int64_t l_prompt, cap;
+  int vpr, l_obs, heads;
+};
+
 __global__ void __launch_bounds__(kCThreads)
 pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ idx_all, int64_t l_prefix,
-                         int radius, int64_t k_sel, int slice) {
+                         int radius, int64_t k_sel, int slice, GatherArgs g) {
   extern __shared__ __align__(16) uint32_t sm[];
   uint32_t* pbits = sm;                                      // [slice] pooled vote bit patterns
   uint32_t* work = sm + round4(slice);                       // 16-B aligned
@@ -223,7 +236,7 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   uint32_t* hist = work;                                     // [kMaxBins] this slice's histogram
   uint32_t* sums = work + round4(max(slice + 2 * radius, kHistWords));   // [2][kMaxBins] cluster histograms
   uint32_t* sh_warp = sums + kSumWords;                      // [32]
-  uint32_t* counts = sh_warp + 32;                           // [8] packed (greater << 16 | equal) per slice
+  uint32_t* counts = sh_warp + 32;                           // [8 + 1] packed (greater << 16 | equal) per slice
   __shared__ uint32_t sh_digit, sh_above;
 
   const int tid = threadIdx.x, lane = tid & 31;
@@ -315,13 +328,23 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   }
   const uint32_t packed = (gt << 16) | eq;
   const uint32_t packed_in = cta_exclusive_scan(packed, sh_warp);
-  if (tid == kCThreads - 1)
-    for (uint32_t r = rank + 1; r < csize; ++r) ptx::dsmem_st_u32(ptx::map_rank(counts + rank, r), packed_in + packed);
+  const uint32_t cta_total = packed_in + packed;   // valid in the last thread
+  if (tid == kCThreads - 1) {
+    for (uint32_t r = rank + 1; r < csize; ++r) ptx::dsmem_st_u32(ptx::map_rank(counts + rank, r), cta_total);
+    counts[kMaxCluster] = cta_total;
+  }
   ptx::cluster_sync();   // last access to another CTA's shared memory
   const uint32_t before = (uint32_t)lane < rank ? counts[lane] : 0u;
   const uint32_t gt_before = warp_sum_u32(before >> 16), eq_before = warp_sum_u32(before & 0xffffu);
   // Output position of this run: every greater value before it, plus the equal values before it
-  // that are kept (the lowest-index need_eq copies of tau are kept).
+  // that are kept (the lowest-index need_eq copies of tau are kept). The CTA's kept rows take the
+  // output positions [p0, p0 + n_kept); `kept` (the histogram space) lists them in order.
+  const uint32_t p0 = gt_before + (eq_before < need_eq ? eq_before : need_eq);
+  const uint32_t eq_cta = counts[kMaxCluster] & 0xffffu;
+  const uint32_t eq_end = eq_before + eq_cta;
+  const uint32_t n_kept = (counts[kMaxCluster] >> 16) + (eq_end < need_eq ? eq_end : need_eq) -
+                          (eq_before < need_eq ? eq_before : need_eq);
+  uint32_t* kept = work;
   const uint32_t e0 = eq_before + (packed_in & 0xffffu);
   uint32_t pos = gt_before + (packed_in >> 16) + (e0 < need_eq ? e0 : need_eq);
   uint32_t e = e0;
@@ -333,16 +356,65 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
       ++e;
     }
     if (keep) {
-      if ((int64_t)pos < k_sel) idx[pos] = j0 + j;
+      if ((int64_t)pos < k_sel) {
+        idx[pos] = j0 + j;
+        kept[pos - p0] = (uint32_t)(j0 + j);
+      }
       ++pos;
     }
   }
+  __syncthreads();
+
+  // Gather: this CTA's kept rows, then window rows rank, rank + csize, ... (16-byte pieces, four
+  // rows' worth of loads in flight per thread).
+  const int vpr = g.vpr;
+  const uint4* kin = g.k + bh * g.l_prompt * vpr;
+  const uint4* vin = g.v + bh * g.l_prompt * vpr;
+  uint4* kout = g.k_out + bh * g.cap * vpr;
+  uint4* vout = g.v_out + bh * g.cap * vpr;
+  const int n_win = (g.l_obs - (int)rank + (int)csize - 1) / (int)csize;   // window rows of this CTA
+  const int64_t items = ((int64_t)n_kept + n_win) * vpr;
+  constexpr int U = 4;
+  for (int64_t base = tid; base < items; base += (int64_t)U * kCThreads) {
+    uint4 kv[U], vv[U];
+    int64_t dst[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t it = base + (int64_t)u * kCThreads;
+      dst[u] = -1;
+      if (it < items) {
+        const int64_t row = it / vpr;
+        const int c = (int)(it - row * vpr);
+        int64_t src, out;
+        if (row < (int64_t)n_kept) {
+          src = kept[row];
+          out = p0 + row;
+        } else {
+          const int64_t t = (int64_t)rank + (row - n_kept) * csize;   // window row
+          src = l_prefix + t;
+          out = k_sel + t;
+        }
+        dst[u] = out * vpr + c;
+        kv[u] = ld_stream_v4(kin + src * vpr + c);
+        vv[u] = ld_stream_v4(vin + src * vpr + c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (dst[u] >= 0) {
+        kout[dst[u]] = kv[u];
+        vout[dst[u]] = vv[u];
+      }
+    }
+  }
+  if (rank == 0 && tid == 0 && bh % g.heads == 0) g.len_out[bh / g.heads] = (int32_t)(k_sel + g.l_obs);
 }
 
 }  // namespace
 
-cudaError_t launch_pool_topk(const CompressJob& job) {
+cudaError_t launch_pool_topk(const CompressJob& job, bool* gathered) {
   const int64_t bh = (int64_t)job.batch * job.heads;
+  if (gathered) *gathered = false;
   job.mark(2 * kStageTopk);
   cudaError_t err = cudaSuccess;
   if (job.k_sel <= 0) {
@@ -354,7 +426,8 @@ cudaError_t launch_pool_topk(const CompressJob& job) {
     const int slice = (int)((job.l_prefix + cl - 1) / cl);
     const int work = slice + 2 * (job.pool_kernel / 2);
     const size_t smem =
-        (size_t)(round4(slice) + round4(work > kHistWords ? work : kHistWords) + kSumWords + 32 + kMaxCluster) * sizeof(uint32_t);
+        (size_t)(round4(slice) + round4(work > kHistWords ? work : kHistWords) + kSumWords + 32 + kMaxCluster + 1) *
+        sizeof(uint32_t);
     err = cudaFuncSetAttribute(pool_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
@@ -369,8 +442,20 @@ cudaError_t launch_pool_topk(const CompressJob& job) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    GatherArgs g;
+    g.k = static_cast<const uint4*>(job.k);
+    g.v = static_cast<const uint4*>(job.v);
+    g.k_out = static_cast<uint4*>(job.k_out);
+    g.v_out = static_cast<uint4*>(job.v_out);
+    g.len_out = job.len_out;
+    g.l_prompt = job.l_prompt;
+    g.cap = job.cap;
+    g.vpr = job.head_dim * (job.dtype == SNAPKV_BF16 ? 2 : 4) / 16;
+    g.l_obs = job.l_obs;
+    g.heads = job.heads;
     err = cudaLaunchKernelEx(&cfg, pool_topk_cluster_kernel, (const float*)job.c, job.idx, job.l_prefix,
-                             job.pool_kernel / 2, job.k_sel, slice);
+                             job.pool_kernel / 2, job.k_sel, slice, g);
+    if (gathered) *gathered = err == cudaSuccess;
   } else {
     pool_topk_kernel<<<(unsigned)bh, kThreads, 0, job.stream>>>(job.c, job.p, job.idx, job.l_prefix,
                                                                 job.pool_kernel / 2, job.k_sel);

@@ -59,7 +59,9 @@ cudaError_t launch_vote_simt(const CompressJob& job);
 bool vote_tc_eligible(const CompressJob& job);
 int vote_tc_keys_per_item(int l_obs);
 cudaError_t launch_vote_tc(const CompressJob& job);
-cudaError_t launch_pool_topk(const CompressJob& job);
+// Max-pool + top-k; for prefixes the cluster kernel handles it also writes K_c, V_c and len_out
+// (*gathered = true), otherwise launch_gather must follow.
+cudaError_t launch_pool_topk(const CompressJob& job, bool* gathered);
 cudaError_t launch_gather(const CompressJob& job);
 
 struct DecodeJob {

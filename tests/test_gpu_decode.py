@@ -150,3 +150,23 @@ def test_decode_garbage_workspace_shared_across_shapes(dev):
         shared = snapkv.decode_attend(q, kc, vc, length, workspace=ws)
         torch.cuda.synchronize()
         assert torch.equal(fresh, shared)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_long_cache_split_path(dev, dtype):
+    """Caches beyond 16K rows take the split kernel (workspace partials + per-head tickets)."""
+    from kv_cache_compression_gb300 import snapkv
+    g = torch.Generator().manual_seed(5)
+    B, H, d, cap = 2, 2, 128, 17000
+    lens = [16999, 9000]
+    kc = torch.randn(B, H, cap, d, generator=g).to(dtype)
+    vc = torch.randn(B, H, cap, d, generator=g).to(dtype)
+    q = (torch.randn(B, H, d, generator=g) * 2).to(dtype)
+    out = snapkv.decode_attend(q.to(dev), kc.to(dev), vc.to(dev), torch.tensor(lens, dtype=torch.int32).to(dev))
+    torch.cuda.synchronize()
+    o = to_numpy_f32(out)
+    for b in range(B):
+        for h in range(H):
+            n = lens[b]
+            ref = orc.decode_attend(q[b, h].float().numpy(), kc[b, h, :n].float().numpy(), vc[b, h, :n].float().numpy())
+            check_decode(o[b, h], ref, dtype == torch.bfloat16, where=f"b{b} h{h} n{n}")

@@ -67,11 +67,22 @@ typedef enum { SNAPKV_SCOPE_PROMPT_CAUSAL = 0, SNAPKV_SCOPE_PREFIX_ONLY = 1 } sn
 
 /* Which kernels compute the logits, softmax statistics and vote (the results agree within the
  * vote tolerance; the selection and the gathered rows are the same up to top-k boundary ties):
- *   AUTO:        the tensor-core kernel when eligible (bf16, L_obs <= 64, at most 2 x SMs items
- *                per head), else the SIMT kernels;
- *   SIMT:        always the SIMT fp32 kernels (any dtype, L_obs <= 128);
- *   TENSOR_CORE: the tensor-core kernel, or SNAPKV_ERR_UNSUPPORTED when not eligible. */
-typedef enum { SNAPKV_ALGO_AUTO = 0, SNAPKV_ALGO_SIMT = 1, SNAPKV_ALGO_TENSOR_CORE = 2 } snapkv_algo;
+ *   AUTO:                the streaming tensor-core kernel when eligible (bf16, L_obs <= 64), else
+ *                        the SIMT kernels;
+ *   SIMT:                always the SIMT fp32 kernels (any dtype, L_obs <= 128);
+ *   TENSOR_CORE:         the streaming tensor-core kernel, or SNAPKV_ERR_UNSUPPORTED when not
+ *                        eligible (its row sums are fp64 atomics, so the vote's last bits can vary
+ *                        from call to call);
+ *   TENSOR_CORE_CLUSTER: one thread-block cluster per head (bf16, L_obs <= 64, a head's keys fit
+ *                        8 CTAs x 4 TMEM slots: L_prompt <= 16384 at L_obs 17..32, 32768 at
+ *                        L_obs <= 16, 8192 at L_obs 33..64), else SNAPKV_ERR_UNSUPPORTED. Every
+ *                        reduction runs in a fixed order, so repeated calls give identical bits. */
+typedef enum {
+  SNAPKV_ALGO_AUTO = 0,
+  SNAPKV_ALGO_SIMT = 1,
+  SNAPKV_ALGO_TENSOR_CORE = 2,
+  SNAPKV_ALGO_TENSOR_CORE_CLUSTER = 3
+} snapkv_algo;
 
 /* Problem statement of one compression call: one layer, `batch` sequences of one length. */
 typedef struct {

@@ -33,7 +33,7 @@ snapkv_status check_params(const snapkv_compress_params* p, int64_t* l_prefix, i
   if (p->softmax_scope != SNAPKV_SCOPE_PROMPT_CAUSAL && p->softmax_scope != SNAPKV_SCOPE_PREFIX_ONLY)
     return SNAPKV_ERR_INVALID_ARG;
   if (p->dtype != SNAPKV_F32 && p->dtype != SNAPKV_BF16) return SNAPKV_ERR_INVALID_ARG;
-  if (p->algo != SNAPKV_ALGO_AUTO && p->algo != SNAPKV_ALGO_SIMT && p->algo != SNAPKV_ALGO_TENSOR_CORE)
+  if (p->algo < SNAPKV_ALGO_AUTO || p->algo > SNAPKV_ALGO_TENSOR_CORE_CLUSTER)
     return SNAPKV_ERR_INVALID_ARG;
   if (p->budget <= 0 && !(p->ratio_p >= 0.0 && p->ratio_p <= 1.0)) return SNAPKV_ERR_INVALID_ARG;
   if ((int64_t)p->batch * p->heads > 65535) return SNAPKV_ERR_INVALID_ARG;  // grid.y limit
@@ -179,17 +179,21 @@ snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, con
   job.events = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(stage_events));
   job.n_events = n_events;
 
-  const bool tc_ok = vote_tc_eligible(job);
-  if (params->algo == SNAPKV_ALGO_TENSOR_CORE && !tc_ok) return SNAPKV_ERR_UNSUPPORTED;
+  const int algo = params->algo;
+  const bool cl_ok = algo == SNAPKV_ALGO_TENSOR_CORE_CLUSTER && vote_cluster_eligible(job);
+  const bool tc_ok = (algo == SNAPKV_ALGO_AUTO || algo == SNAPKV_ALGO_TENSOR_CORE) && vote_tc_eligible(job);
+  const bool tc_only = algo == SNAPKV_ALGO_TENSOR_CORE || algo == SNAPKV_ALGO_TENSOR_CORE_CLUSTER;
+  if (tc_only && !cl_ok && !tc_ok) return SNAPKV_ERR_UNSUPPORTED;
   bool voted = false;
-  if (tc_ok && params->algo != SNAPKV_ALGO_SIMT) {
-    if (launch_vote_tc(job) == cudaSuccess) {
-      voted = true;
-    } else {
-      cudaGetLastError();   // a refused cooperative launch is not sticky; use the SIMT kernels
-      if (params->algo == SNAPKV_ALGO_TENSOR_CORE) return SNAPKV_ERR_CUDA;
-    }
+  if (cl_ok) {
+    if (launch_vote_cluster(job) == cudaSuccess) voted = true;
+    else cudaGetLastError();   // a refused launch is not sticky; try the next kernel
   }
+  if (!voted && tc_ok) {
+    if (launch_vote_tc(job) == cudaSuccess) voted = true;
+    else cudaGetLastError();
+  }
+  if (!voted && tc_only) return SNAPKV_ERR_CUDA;
   if (!voted && launch_vote_simt(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
   bool gathered = false;
   if (launch_pool_topk(job, &gathered) != cudaSuccess) return SNAPKV_ERR_CUDA;

@@ -57,6 +57,9 @@ CompressLayout compress_layout(int batch, int heads, int l_obs, int64_t l_prompt
 cudaError_t launch_vote_simt(const CompressJob& job);
 // Tensor-core score + vote (bf16, d 64/128, L_obs <= 64, items per head <= 2 x SMs).
 bool vote_tc_eligible(const CompressJob& job);
+// The cluster-per-head tensor-core kernel (a head's keys fit 8 CTAs x 4 TMEM slots).
+bool vote_cluster_eligible(const CompressJob& job);
+cudaError_t launch_vote_cluster(const CompressJob& job);
 int vote_tc_keys_per_item(int l_obs);
 cudaError_t launch_vote_tc(const CompressJob& job);
 // Max-pool + top-k; for prefixes the cluster kernel handles it also writes K_c, V_c and len_out

@@ -42,6 +42,7 @@
 #include "sm100_ptx.cuh"
 #include "snapkv_common.cuh"
 #include "snapkv_internal.h"
+#include "tc_common.cuh"
 
 namespace snapkv {
 namespace {
@@ -154,48 +155,6 @@ __device__ __forceinline__ int tiles_of(const TcArgs& a, int chunk, int TI) {
   const int64_t left = a.l_prompt - key0;
   const int t = (int)((left + kTileKeys - 1) / kTileKeys);
   return t < TI ? t : TI;
-}
-
-// Butterfly reduce-transpose of C per-lane values over the 32 lanes of a warp (max or sum):
-// afterwards lane l holds the warp-wide result of row l (C == 32) or of row l/2 (C == 16) in v[0].
-template <int C, int O>
-__device__ __forceinline__ void butterfly_max(float* v, int lane) {
-  if constexpr (O >= 1) {
-    if constexpr (C >= 2) {
-      constexpr int H = C / 2;
-      const bool upper = (lane & O) != 0;
-#pragma unroll
-      for (int k = 0; k < H; ++k) {
-        const float send = upper ? v[k] : v[k + H];
-        const float keep = upper ? v[k + H] : v[k];
-        v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, O));
-      }
-      butterfly_max<H, O / 2>(v, lane);
-    } else {
-      v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], O));
-      butterfly_max<1, O / 2>(v, lane);
-    }
-  }
-}
-
-template <int C, int O>
-__device__ __forceinline__ void butterfly_sum(float* v, int lane) {
-  if constexpr (O >= 1) {
-    if constexpr (C >= 2) {
-      constexpr int H = C / 2;
-      const bool upper = (lane & O) != 0;
-#pragma unroll
-      for (int k = 0; k < H; ++k) {
-        const float send = upper ? v[k] : v[k + H];
-        const float keep = upper ? v[k + H] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, O);
-      }
-      butterfly_sum<H, O / 2>(v, lane);
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-      butterfly_sum<1, O / 2>(v, lane);
-    }
-  }
 }
 
 template <int D, int N>
@@ -417,7 +376,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
             }
           }
         }
-        butterfly_max<R, 16>(v, lane);
+        tc::butterfly_max<R, 16>(v, lane);
         stash_rows(v, r0);
         ptx::named_barrier(bar_id, 128);
         if (gtid < R) {
@@ -452,7 +411,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         }
         const bool last_read = !a.resident && r0 + R >= N;   // resident items keep the slot
         if (last_read) ptx::tc_fence_before();
-        butterfly_sum<R, 16>(v, lane);
+        tc::butterfly_sum<R, 16>(v, lane);
         stash_rows(v, r0);
         ptx::named_barrier(bar_id, 128);
         if (last_read && gtid == 0) ptx::mbar_arrive(&c.tmem_empty[slot]);
@@ -568,31 +527,6 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-bool make_map(CUtensorMap* map, const void* ptr, int d, int64_t rows, int64_t heads, int box_rows) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
-  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, int N>
 cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   using Lay = TcLayout<D, N>;
@@ -601,7 +535,7 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   cudaError_t err;
   CUtensorMap mk, mq;
   const int64_t bh = (int64_t)job.batch * job.heads;
-  if (!make_map(&mk, job.k, D, job.l_prompt, bh, kTileKeys) || !make_map(&mq, job.q_obs, D, job.l_obs, bh, N))
+  if (!tc::make_map(&mk, job.k, D, job.l_prompt, bh, kTileKeys) || !tc::make_map(&mq, job.q_obs, D, job.l_obs, bh, N))
     return cudaErrorInvalidValue;
   TcArgs a;
   a.l_prompt = job.l_prompt;

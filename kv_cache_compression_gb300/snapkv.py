@@ -23,8 +23,9 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT, ERR_W
     0, 1, 2, 4, 8, 16, 32, 64)
 F32, BF16 = 0, 1
 SCOPE_PROMPT_CAUSAL, SCOPE_PREFIX_ONLY = 0, 1
-ALGO_AUTO, ALGO_SIMT, ALGO_TENSOR_CORE = 0, 1, 2
-_ALGOS = {"auto": ALGO_AUTO, "simt": ALGO_SIMT, "tensor_core": ALGO_TENSOR_CORE}
+ALGO_AUTO, ALGO_SIMT, ALGO_TENSOR_CORE, ALGO_TENSOR_CORE_CLUSTER = 0, 1, 2, 3
+_ALGOS = {"auto": ALGO_AUTO, "simt": ALGO_SIMT, "tensor_core": ALGO_TENSOR_CORE,
+          "tensor_core_cluster": ALGO_TENSOR_CORE_CLUSTER}
 _SCOPES = {"prompt_causal": SCOPE_PROMPT_CAUSAL, "prefix_only": SCOPE_PREFIX_ONLY}
 
 

@@ -86,7 +86,7 @@ def test_compress_rejects_bad_arguments_before_launch(lib):
     assert _call_compress(lib, _params(l_obs=0)) == sk.ERR_INVALID_ARG
     assert _call_compress(lib, _params(scope="prefix_only", dtype=7)) == sk.ERR_INVALID_ARG
     bad = _params()
-    bad.algo = 3
+    bad.algo = 4
     assert _call_compress(lib, bad) == sk.ERR_INVALID_ARG
 
 

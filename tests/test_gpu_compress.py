@@ -61,7 +61,7 @@ def test_tiny_fp32_prefix_only_scope(dev):
     _run_workload(dev, synth.WORKLOADS[0], scope="prefix_only")
 
 
-@pytest.mark.parametrize("algo", ["tensor_core", "simt"])
+@pytest.mark.parametrize("algo", ["tensor_core", "tensor_core_cluster", "simt"])
 def test_llama_layer_every_head(dev, algo):
     _, excused = _run_workload(dev, synth.WORKLOADS[1], algo=algo)
     print(f"boundary-excused indices ({algo}): {excused}")
@@ -104,10 +104,12 @@ EDGE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("algo", ["auto", "simt"])
+@pytest.mark.parametrize("algo", ["auto", "tensor_core_cluster", "simt"])
 @pytest.mark.parametrize("case", EDGE_CASES, ids=lambda c: f"bf16={c[0]}-d{c[1]}-obs{c[2]}-K{c[3]}-L{c[4]}")
 def test_edge_cases(dev, case, algo):
     bf16, d, l_obs, pool, L, p, budget, scope, B, H = case
+    if algo == "tensor_core_cluster" and (not bf16 or l_obs > 64):
+        pytest.skip("the cluster tensor-core kernel takes bf16 with L_obs <= 64")
     wl = synth.Workload("edge", 40 + L % 17, bf16=bf16, batch=B, heads=H, head_dim=d, layers=1, l_prompt=L,
                         l_obs=l_obs, pool_kernel=pool, ratio_p=p, budget=budget)
     _run_workload(dev, wl, scope=scope, algo=algo)
@@ -122,7 +124,7 @@ def test_tensor_core_path_is_refused_when_ineligible(dev):
     assert e.value.status == snapkv.ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("algo", ["tensor_core", "simt"])
+@pytest.mark.parametrize("algo", ["tensor_core", "tensor_core_cluster", "simt"])
 def test_zero_queries_keep_the_first_k(dev, algo):
     """q = 0 makes every pooled score equal; ties go to the lower index, so I = 0..k-1 exactly."""
     from kv_cache_compression_gb300 import snapkv
@@ -135,21 +137,24 @@ def test_zero_queries_keep_the_first_k(dev, algo):
         assert res["idx"][0, h].cpu().tolist() == list(range(300))
 
 
-def test_workspace_is_reusable(dev):
+@pytest.mark.parametrize("algo", ["auto", "tensor_core_cluster"])
+def test_workspace_is_reusable(dev, algo):
     from kv_cache_compression_gb300 import snapkv
     wl = synth.WORKLOADS[1].with_(heads=4, l_prompt=4096)
     q, k, v, _ = synth.device_inputs(wl, 0, 0, 1, wl.l_prompt, dev)
-    first = snapkv.compress(q, k, v, pool_kernel=7, budget=wl.budget, want_vote=True)
-    again = snapkv.compress(q, k, v, pool_kernel=7, budget=wl.budget, want_vote=True, workspace=first["workspace"])
+    first = snapkv.compress(q, k, v, pool_kernel=7, budget=wl.budget, algo=algo, want_vote=True)
+    again = snapkv.compress(q, k, v, pool_kernel=7, budget=wl.budget, algo=algo, want_vote=True,
+                            workspace=first["workspace"])
     torch.cuda.synchronize()
-    # The tensor-core path sums each row's exponentials with fp64 atomics, whose order varies from
-    # run to run, so the vote may differ in its last bits; the selection and the copies do not.
-    assert torch.allclose(first["vote"], again["vote"], rtol=1e-6, atol=0)
+    if algo == "tensor_core_cluster":   # row sums folded in a fixed order: bit for bit
+        assert torch.equal(first["vote"], again["vote"])
+    else:   # the streaming kernel adds them with fp64 atomics in a varying order
+        assert torch.allclose(first["vote"], again["vote"], rtol=1e-6, atol=0)
     assert torch.equal(first["idx"], again["idx"])
     assert torch.equal(first["k_out"], again["k_out"])
 
 
-@pytest.mark.parametrize("algo", ["auto", "simt"])
+@pytest.mark.parametrize("algo", ["auto", "tensor_core_cluster", "simt"])
 def test_garbage_workspace_shared_across_shapes(dev, algo):
     """The workspace is scratch: random contents, and reuse by a call of another shape, change nothing."""
     from kv_cache_compression_gb300 import snapkv
@@ -167,11 +172,11 @@ def test_garbage_workspace_shared_across_shapes(dev, algo):
             fresh = snapkv.compress(q, k, v, pool_kernel=pk, budget=wl.budget, algo=algo, want_vote=True)
             shared = snapkv.compress(q, k, v, pool_kernel=pk, budget=wl.budget, algo=algo, want_vote=True, workspace=ws)
             torch.cuda.synchronize()
-            if algo == "simt":   # fixed summation order: bit for bit
+            if algo in ("simt", "tensor_core_cluster"):   # fixed summation order: bit for bit
                 assert torch.equal(fresh["vote"], shared["vote"])
                 assert torch.equal(fresh["idx"], shared["idx"])
                 assert torch.equal(fresh["k_out"], shared["k_out"]) and torch.equal(fresh["v_out"], shared["v_out"])
-            else:                # fp64 atomics in a varying order: the last bits of the vote may differ
+            else:   # the streaming kernel adds with fp64 atomics in a varying order: last bits may differ
                 assert torch.allclose(fresh["vote"], shared["vote"], rtol=1e-6, atol=0)
             for h in range(wl.heads):
                 hi = synth.host_head(wl, round_, 0, h, l_prompt=wl.l_prompt)

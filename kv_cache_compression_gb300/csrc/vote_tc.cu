@@ -110,11 +110,13 @@ struct TcLayout {
   static constexpr int STAGE_BYTES = KB * A_BYTES;
   static constexpr int QB_BYTES = N * 128;          // one k-block of the window queries
   static constexpr int Q_BYTES = KB * QB_BYTES;
-  // Everything but the key-tile ring, then as many ring stages as the 227 KB of shared memory
-  // allow (at most 8): more bytes in flight per SM keep HBM busy at loaded-memory latency.
+  // Everything but the key-tile ring, then at most 3 ring stages: 152 SMs x 3 x 32 KB of reads in
+  // flight already keep HBM busy, and a deeper ring only lengthens the memory queues that the
+  // epilogue's reductions, counter updates and vote stores wait in (8 stages: 39.3 us per launch
+  // of the 16K-key layer, 3 stages: 34.6 us).
   static constexpr int FIXED = 2 * Q_BYTES + 2 * 4 * N * 4 + 2 * N * 4 + 8 * (2 * 8 + 4 + 4 * 16 + 4 + 1) + 64 + 1024;
   static constexpr int STAGES_FIT = (232448 - FIXED) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT < 8 ? STAGES_FIT : 8;
+  static constexpr int STAGES = STAGES_FIT < 3 ? STAGES_FIT : 3;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_Q = OFF_K + STAGES * STAGE_BYTES;
   static constexpr int OFF_RED = OFF_Q + 2 * Q_BYTES;        // [2 groups][4 warps][N] floats

@@ -243,14 +243,26 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecArgs a) {
 }
 
 // One cluster per (sequence, head): CTA `rank` takes rows [rank * per, (rank + 1) * per) of the
-// head's cap rows (those at or past len masked), with up to UNROLL rows per lane group in flight.
+// head's cap rows (those at or past len masked). The rows are contiguous in the cache, so one
+// thread streams them into shared memory with bulk copies, kClBufs chunks of 16 KB of K and 16 KB
+// of V in flight, and the row groups compute from shared memory.
+constexpr int kClChunkBytes = 16 * 1024;
+constexpr int kClBufs = 3;
+constexpr long long kClWaitLimit = 4000000000LL;   // ~2 s of SM clock
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(DecArgs a) {
   constexpr int V = Elem<T>::kVec;
   constexpr int LPR = D / V;                       // lanes per cache row
   constexpr int RPW = 32 / LPR;                    // rows per warp step
   constexpr int GROUPS = (kClThreads / 32) * RPW;  // row groups per CTA
-  constexpr int UNROLL = 8;
+  constexpr int ROW_BYTES = D * (int)sizeof(T);
+  constexpr int CH = kClChunkBytes / ROW_BYTES;    // rows per chunk
+  constexpr int UNROLL = CH / GROUPS;              // rows per group per chunk
+  static_assert(CH % GROUPS == 0, "chunk rows");
+  extern __shared__ __align__(128) uint8_t dsm[];  // [kClBufs][K, V][kClChunkBytes]
+  __shared__ __align__(8) uint64_t bar[kClBufs];
+  __shared__ int no_abort;
   __shared__ float sm_m[GROUPS], sm_l[GROUPS];
   __shared__ __align__(16) float sm_o[GROUPS][D];
   __shared__ float cta_m, cta_l;                   // this CTA's partial, read by the whole cluster
@@ -260,16 +272,36 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(DecArgs a) {
   const uint32_t rank = ptx::cluster_rank(), csize = ptx::cluster_size();
   const int64_t bh = blockIdx.x / csize;
   const int b = (int)(bh / a.heads);
-  int n = a.len[b];
-  if ((int64_t)n > a.cap) {
-    if (rank == 0 && tid == 0 && bh % a.heads == 0) report(a.dev_status, SNAPKV_ERR_CAPACITY);
-    n = (int)a.cap;
-  }
-  if (n < 0) n = 0;
   const int cap = (int)a.cap;
   const int per = (cap + (int)csize - 1) / (int)csize;
   const int r0 = min(cap, (int)rank * per);
-  const int r1 = min(cap, r0 + per);   // rows at or past n are loaded (they are inside cap) and masked
+  const int r1 = min(cap, r0 + per);   // rows at or past n are streamed (they are inside cap) and masked
+  const int nchunks = (r1 - r0 + CH - 1) / CH;
+  const T* kc = static_cast<const T*>(a.k_cache) + bh * a.cap * D;
+  const T* vc = static_cast<const T*>(a.v_cache) + bh * a.cap * D;
+  auto issue = [&](int c) {
+    const int buf = c % kClBufs;
+    const int cr0 = r0 + c * CH;
+    const uint32_t bytes = (uint32_t)(min(CH, r1 - cr0) * ROW_BYTES);
+    ptx::mbar_arrive_expect_tx(&bar[buf], 2 * bytes);
+    ptx::bulk_load(dsm + (2 * buf) * kClChunkBytes, kc + (int64_t)cr0 * D, bytes, &bar[buf]);
+    ptx::bulk_load(dsm + (2 * buf + 1) * kClChunkBytes, vc + (int64_t)cr0 * D, bytes, &bar[buf]);
+  };
+  if (tid == 0) {
+    for (int i = 0; i < kClBufs; ++i) ptx::mbar_init(&bar[i], 1);
+    no_abort = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int c = 0; c < nchunks && c < kClBufs; ++c) issue(c);
+
+  int n = a.len[b];
+  if ((int64_t)n > a.cap) {
+    if (rank == 0 && tid == 0 && bh % a.heads == 0) report(a.dev_status, SNAPKV_ERR_CAPACITY);
+    n = cap;
+  }
+  if (n < 0) n = 0;
   const int sub = lane / LPR, cl = lane % LPR;
   const int group = warp * RPW + sub;
 
@@ -279,59 +311,59 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(DecArgs a) {
 #pragma unroll
   for (int e = 0; e < V; ++e) q[e] *= a.scale_log2;
 
-  const T* kc = static_cast<const T*>(a.k_cache) + bh * a.cap * D + cl * V;
-  const T* vc = static_cast<const T*>(a.v_cache) + bh * a.cap * D + cl * V;
   float m = -INFINITY, l = 0.f, o[V];
 #pragma unroll
   for (int e = 0; e < V; ++e) o[e] = 0.f;
-
-  // The trip count depends only on the CTA's range, so every lane of a warp runs the same
-  // iterations (the row reductions below shuffle across the whole warp).
-  for (int base = r0; base < r1; base += GROUPS * UNROLL) {
-    const int rb = base + group;
-    uint4 kr[UNROLL], vr[UNROLL];
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const int r = rb + u * GROUPS;
-      if (r < r1) {
-        kr[u] = ld_stream_v4(kc + (int64_t)r * D);
-        vr[u] = ld_stream_v4(vc + (int64_t)r * D);
-      } else {
-        kr[u] = make_uint4(0, 0, 0, 0);
-        vr[u] = make_uint4(0, 0, 0, 0);
-      }
-    }
+  bool timed_out = false;
+  for (int c = 0; c < nchunks; ++c) {
+    const int buf = c % kClBufs;
+    if (!ptx::mbar_wait(&bar[buf], (uint32_t)((c / kClBufs) & 1), &no_abort, kClWaitLimit)) timed_out = true;
+    const uint8_t* kbuf = dsm + (2 * buf) * kClChunkBytes;
+    const uint8_t* vbuf = kbuf + kClChunkBytes;
+    const int cr0 = r0 + c * CH;
     float s[UNROLL];
     float smax = -INFINITY;
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
+      const int rr = group + u * GROUPS;   // row within the chunk
       float kf[V];
-      Elem<T>::widen(kr[u], kf);
+      Elem<T>::widen(*reinterpret_cast<const uint4*>(kbuf + rr * ROW_BYTES + cl * 16), kf);
       float dot = 0.f;
 #pragma unroll
       for (int e = 0; e < V; ++e) dot = fmaf(q[e], kf[e], dot);
 #pragma unroll
       for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-      const int r = rb + u * GROUPS;
+      const int r = cr0 + rr;
       s[u] = (r < r1 && r < n) ? dot : -INFINITY;
       smax = fmaxf(smax, s[u]);
     }
     const float m_new = fmaxf(m, smax);
-    if (m_new == -INFINITY) continue;
-    const float corr = ex2(m - m_new);
-    l *= corr;
+    if (m_new != -INFINITY) {
+      const float corr = ex2(m - m_new);
+      l *= corr;
 #pragma unroll
-    for (int e = 0; e < V; ++e) o[e] *= corr;
+      for (int e = 0; e < V; ++e) o[e] *= corr;
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const float p = ex2(s[u] - m_new);   // 0 for masked rows
-      float vf[V];
-      Elem<T>::widen(vr[u], vf);
-      l += p;
+      for (int u = 0; u < UNROLL; ++u) {
+        const float p = ex2(s[u] - m_new);   // 0 for masked rows
+        if (p != 0.f) {
+          float vf[V];
+          Elem<T>::widen(*reinterpret_cast<const uint4*>(vbuf + (group + u * GROUPS) * ROW_BYTES + cl * 16), vf);
+          l += p;
 #pragma unroll
-      for (int e = 0; e < V; ++e) o[e] = fmaf(p, vf[e], o[e]);
+          for (int e = 0; e < V; ++e) o[e] = fmaf(p, vf[e], o[e]);
+        }
+      }
+      m = m_new;
     }
-    m = m_new;
+    __syncthreads();   // every group is done with this buffer
+    if (tid == 0 && c + kClBufs < nchunks) issue(c + kClBufs);
+  }
+  if (timed_out && tid == 0) {
+    report(a.dev_status, SNAPKV_ERR_TIMEOUT);
+    // A copy whose wait gave up may still be landing: wait for it (bounded) before leaving.
+    for (int c = (nchunks > kClBufs ? nchunks - kClBufs : 0); c < nchunks; ++c)
+      ptx::mbar_wait(&bar[c % kClBufs], (uint32_t)((c / kClBufs) & 1), &no_abort, kClWaitLimit);
   }
 
   if (cl == 0) {
@@ -394,9 +426,16 @@ cudaError_t launch_decode_cluster(const DecodeJob& job, const DecArgs& a) {
   if (csize > kClMaxCtas) csize = kClMaxCtas;
   if (csize < 1) csize = 1;
   cudaLaunchConfig_t cfg = {};
+  static std::once_flag smem_set;   // the dynamic shared-memory attribute, once per instantiation
+  static cudaError_t smem_err = cudaSuccess;
+  std::call_once(smem_set, [] {
+    smem_err = cudaFuncSetAttribute(decode_cluster_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    2 * kClBufs * kClChunkBytes);
+  });
+  if (smem_err != cudaSuccess) return smem_err;
   cfg.gridDim = dim3((unsigned)(bh * csize));
   cfg.blockDim = dim3(kClThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = 2 * kClBufs * kClChunkBytes;
   cfg.stream = job.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

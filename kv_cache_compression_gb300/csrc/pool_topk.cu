@@ -237,7 +237,7 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   uint32_t* sums = work + round4(max(slice + 2 * radius, kHistWords));   // [2][kMaxBins] cluster histograms
   uint32_t* sh_warp = sums + kSumWords;                      // [32]
   uint32_t* counts = sh_warp + 32;                           // [8 + 1] packed (greater << 16 | equal) per slice
-  __shared__ uint32_t sh_digit, sh_above;
+  __shared__ uint32_t sh_digit, sh_above, sh_full;
 
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t rank = ptx::cluster_rank(), csize = ptx::cluster_size();
@@ -301,6 +301,7 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
         if (acc + hb[q] >= krem) {
           sh_digit = (uint32_t)(4 * g + 3 - q);
           sh_above = acc;
+          sh_full = acc + hb[q] == krem ? 1u : 0u;   // the digit's bin is kept whole
           break;
         }
         acc += hb[q];
@@ -310,9 +311,14 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
     prefix |= sh_digit << shift;
     mask |= (uint32_t)(nb - 1) << shift;
     krem -= sh_above;
+    // When every value with the digits found so far is kept, the lower digits cannot change the
+    // selection: stop (every CTA reads the same histogram, so all stop at the same pass).
+    if (sh_full) break;
     if (pass == 0)   // cleared before this CTA arrives at the next pass's barrier
       for (int b = tid; b < nb; b += kCThreads) s[b] = 0u;
   }
+  // Selection: every value whose decided digits exceed tau's, plus the lowest-index need_eq of
+  // those equal to tau's (all of them when the select stopped early).
   const uint32_t tau = prefix, need_eq = krem;
 
   // Ordered compaction: thread = contiguous run of the slice; slices in rank order. A slice holds
@@ -322,7 +328,7 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   const int a0 = min(n, tid * per), a1 = min(n, a0 + per);
   uint32_t gt = 0, eq = 0;
   for (int j = a0; j < a1; ++j) {
-    const uint32_t u = pbits[j];
+    const uint32_t u = pbits[j] & mask;
     gt += u > tau;
     eq += u == tau;
   }
@@ -349,7 +355,7 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   uint32_t pos = gt_before + (packed_in >> 16) + (e0 < need_eq ? e0 : need_eq);
   uint32_t e = e0;
   for (int j = a0; j < a1; ++j) {
-    const uint32_t u = pbits[j];
+    const uint32_t u = pbits[j] & mask;
     bool keep = u > tau;
     if (u == tau) {
       keep = e < need_eq;

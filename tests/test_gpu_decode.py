@@ -170,3 +170,29 @@ def test_decode_long_cache_split_path(dev, dtype):
             n = lens[b]
             ref = orc.decode_attend(q[b, h].float().numpy(), kc[b, h, :n].float().numpy(), vc[b, h, :n].float().numpy())
             check_decode(o[b, h], ref, dtype == torch.bfloat16, where=f"b{b} h{h} n{n}")
+
+
+@pytest.mark.parametrize("extra", [0, 1])
+def test_full_16k_cache_decode_sampled(dev, extra):
+    """Decode over an uncompressed 16K-row prompt cache (batch 2), the baseline the compressed
+    cache is compared with: cap 16384 takes the cluster kernel, cap 16385 the split kernel."""
+    from kv_cache_compression_gb300 import snapkv
+    wl = synth.WORKLOADS[1]
+    B, L = 2, wl.l_prompt
+    _, k, v, _ = synth.device_inputs(wl, 0, 0, B, L, dev)
+    qn, kn, vn = synth.device_decode_tokens(wl, 0, 0, 0, B, dev)
+    cap = L + extra
+    kc = torch.zeros((B, wl.heads, cap, wl.head_dim), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    kc[:, :, :L] = k
+    vc[:, :, :L] = v
+    length = torch.full((B,), L, dtype=torch.int32, device=dev)
+    if extra:   # append the new token first, as a decode step does
+        snapkv.append(kn, vn, kc, vc, length)
+    out = snapkv.decode_attend(qn, kc, vc, length)
+    torch.cuda.synchronize()
+    n = L + extra
+    o = to_numpy_f32(out)
+    for b, h in [(0, 0), (1, 17), (1, 31)]:
+        ref = orc.decode_attend(to_numpy_f32(qn[b, h]), to_numpy_f32(kc[b, h, :n]), to_numpy_f32(vc[b, h, :n]))
+        check_decode(o[b, h], ref, True, where=f"b{b} h{h} n{n}")

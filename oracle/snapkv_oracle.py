@@ -221,6 +221,32 @@ def decode_attend(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray) -> np
     return w @ np.asarray(v_cache, dtype=np.float64)
 
 
+@dataclass
+class HitCount:
+    hits: int       # sum of O = M_threshold AND M_vote over the prefix positions
+    total: int      # sum of M_threshold
+    weights: np.ndarray   # A_cur over the prefix positions (float64), for boundary checks
+
+
+def hit_count(q: np.ndarray, k_cache: np.ndarray, l_prefix: int, idx: np.ndarray, theta: float = 0.05) -> HitCount:
+    """[SnapKV] Hit Rate（適中率）の定式化, for one head and one generation-time query.
+
+    A_cur is the query's attention over every cached row (softmax of q K^T / sqrt(d), the decode
+    attention of [KVcache] 22.2) taken at the prefix positions j < l_prefix; M_threshold marks
+    A_cur > theta, M_vote marks the kept positions idx, O = M_threshold AND M_vote, and the hit
+    rate is H = sum(O) / sum(M_threshold) (summed over heads by the caller).
+    """
+    q64 = np.asarray(q, dtype=np.float64)
+    s = (np.asarray(k_cache, dtype=np.float64) @ q64) / math.sqrt(q64.shape[0])
+    w = np.exp(s - s.max())
+    w = w / w.sum()
+    a_cur = w[:l_prefix]
+    m_thr = a_cur > theta
+    m_vote = np.zeros(a_cur.shape[0], dtype=bool)
+    m_vote[np.asarray(idx, dtype=np.int64)] = True
+    return HitCount(hits=int(np.sum(m_thr & m_vote)), total=int(np.sum(m_thr)), weights=a_cur)
+
+
 def kv_cache_bytes(batch: int, seq: int, layers: int, kv_heads: int, head_dim: int,
                    elem_bytes: int) -> int:
     """[KVcache] 22.4: M_KV = 2 B S L H_KV d_h b (dense cache, keys and values)."""

@@ -2,7 +2,8 @@
 
 Shows that the pins in test_oracle_pins.py are sensitive to the plausible mistakes: a dropped
 scale, an off-by-one causal mask, a wrong pool radius, the wrong tie rule, a wrong sum bound,
-a transposed decode operand.
+a transposed decode operand, an inclusive hit-rate threshold, hit-rate attention counted
+outside the prefix.
 """
 import math
 
@@ -71,3 +72,36 @@ def test_transposed_decode_operand_is_caught(monkeypatch):
     monkeypatch.setattr(orc, "decode_attend", bad_decode)
     worst, _ = pins.pin_decode_vs_full_causal(orc, x[0], x[1], x[2], l_prompt=3)
     assert worst > 1e-3
+
+
+def _hit_count_variant(inclusive=False, whole_cache=False):
+    """hit_count with a planted mistake: >= theta instead of > theta, or no restriction to the prefix."""
+    def bad(q, k_cache, l_prefix, idx, theta=0.05):
+        q64 = np.asarray(q, dtype=np.float64)
+        s = (np.asarray(k_cache, dtype=np.float64) @ q64) / math.sqrt(q64.shape[0])
+        w = np.exp(s - s.max())
+        w = w / w.sum()
+        a_cur = w if whole_cache else w[:l_prefix]
+        m_thr = a_cur >= theta if inclusive else a_cur > theta
+        m_vote = np.zeros(a_cur.shape[0], dtype=bool)
+        m_vote[np.asarray(idx, dtype=np.int64)] = True
+        return orc.HitCount(hits=int(np.sum(m_thr & m_vote)), total=int(np.sum(m_thr)), weights=a_cur)
+    return bad
+
+
+def test_inclusive_hit_threshold_is_caught(monkeypatch):
+    monkeypatch.setattr(orc, "hit_count", _hit_count_variant(inclusive=True))
+    try:
+        pins.test_hit_count_uniform_weights_and_strict_threshold()
+    except AssertionError:
+        return
+    raise AssertionError("the pin did not catch an inclusive threshold")
+
+
+def test_hit_count_over_the_window_is_caught(monkeypatch):
+    monkeypatch.setattr(orc, "hit_count", _hit_count_variant(whole_cache=True))
+    try:
+        pins.test_hit_count_dominant_key_and_prefix_restriction()
+    except AssertionError:
+        return
+    raise AssertionError("the pin did not catch attention counted outside the prefix")

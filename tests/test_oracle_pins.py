@@ -376,3 +376,51 @@ def test_kv_cache_bytes_matches_worked_example():
                               g["elem_bytes"]) == g["bytes_at_tokens"]
     for s, b in g["extrapolated"].items():
         assert orc.kv_cache_bytes(1, int(s), 32, 32, 128, 2) == b
+
+
+# ------------------------------------------------------------------------------------------------
+# Hit rate ([SnapKV] Hit Rate（適中率）の定式化)
+# ------------------------------------------------------------------------------------------------
+
+def test_hit_count_threshold_zero_counts_every_prefix_position():
+    """theta = 0: every prefix weight is positive, so M_threshold covers the prefix and the hits are
+    exactly the kept positions."""
+    rng = np.random.default_rng(41)
+    k = _rand(rng, 40, 16)
+    q = _rand(rng, 16)
+    idx = np.array([1, 5, 9, 30])
+    h = orc.hit_count(q, k, 33, idx, theta=0.0)
+    assert (h.total, h.hits) == (33, 4)
+
+
+def test_hit_count_keeping_the_whole_prefix_hits_everything():
+    rng = np.random.default_rng(42)
+    k = _rand(rng, 50, 8, scale=3.0)
+    q = _rand(rng, 8)
+    h = orc.hit_count(q, k, 45, np.arange(45), theta=0.01)
+    assert h.total > 0 and h.hits == h.total
+
+
+def test_hit_count_uniform_weights_and_strict_threshold():
+    """q = 0 gives every cached row the weight 1/len exactly (len = 64 is a power of two): the mask
+    keeps weights strictly above theta, so theta = 1/len marks nothing and just below it everything."""
+    k = np.random.default_rng(43).standard_normal((64, 8))
+    q = np.zeros(8)
+    assert orc.hit_count(q, k, 60, np.arange(10), theta=1.0 / 64).total == 0
+    h = orc.hit_count(q, k, 60, np.arange(10), theta=1.0 / 64 - 1e-12)
+    assert (h.total, h.hits) == (60, 10)
+
+
+def test_hit_count_dominant_key_and_prefix_restriction():
+    """One key aligned with a long query takes almost all the weight: it is the only position above
+    theta. Inside the prefix it counts (a hit only if kept); in the window it does not count."""
+    rng = np.random.default_rng(44)
+    d, n, l_prefix = 16, 48, 40
+    k = _rand(rng, n, d, scale=0.1)
+    q = np.zeros(d)
+    q[0] = 50.0
+    for jstar, kept, want in [(7, [7, 20], (1, 1)), (7, [3, 20], (0, 1)), (44, [3, 20], (0, 0))]:
+        kk = k.copy()
+        kk[jstar, 0] = 5.0
+        h = orc.hit_count(q, kk, l_prefix, np.array(kept), theta=0.05)
+        assert (h.hits, h.total) == want, (jstar, kept)

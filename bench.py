@@ -325,6 +325,34 @@ def full_cache_decode(torch, snapkv, synth, dev, ksel_budget=1024):
     return res
 
 
+def hit_rate_diagnostic(torch, snapkv, synth, dev, q, k, v, wl, theta=0.05):
+    """The explainer's Hit Rate (section Hit Rate（適中率）の定式化) of the bench workload's selection:
+    a decode-step query over the uncompressed cache (prompt + the new row), theta = 0.05, summed
+    over the 32 heads; plus the diagnostic kernel's time (mean of 20 calls between events)."""
+    res = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, budget=wl.budget)
+    qn, kn, _ = synth.device_decode_tokens(wl, 0, 0, 0, 1, dev)
+    cache = torch.cat([k, kn[:, :, None, :]], dim=2).contiguous()
+    length = torch.full((1,), wl.l_prompt + 1, dtype=torch.int32, device=dev)
+    l_prefix = wl.l_prompt - wl.l_obs
+    hits, total = snapkv.hit_rate(qn, cache, length, res["idx"], l_prefix, theta=theta)
+    # a finer threshold too: independent random queries spread their weight thinly over 16K keys
+    fine = 4.0 / wl.l_prompt
+    hf, tf = snapkv.hit_rate(qn, cache, length, res["idx"], l_prefix, theta=fine)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(20):
+        snapkv.hit_rate(qn, cache, length, res["idx"], l_prefix, theta=theta)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    h, t = int(hits.sum().item()), int(total.sum().item())
+    h2, t2 = int(hf.sum().item()), int(tf.sum().item())
+    ms = e0.elapsed_time(e1) / 20
+    return {"H": (h / t) if t else None, "hits": h, "above_theta": t, "theta": theta,
+            "H_fine": (h2 / t2) if t2 else None, "above_fine": t2, "theta_fine": fine,
+            "kernel_ms": ms, "kernel_alg_gbs": 32 * (wl.l_prompt + 1) * wl.head_dim * 2 / (ms * 1e-3) / 1e9,
+            "note": "synthetic inputs: the value describes these tensors, not a trained model"}
+
+
 def timing_event(torch):
     """A timing event that, recorded inside a stream capture, becomes an event-record node."""
     try:
@@ -556,6 +584,7 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     full_cache = full_cache_decode(torch, snapkv, synth, dev) if world == 1 else None
+    hit = hit_rate_diagnostic(torch, snapkv, synth, dev, *copies[0], wl) if world == 1 else None
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
@@ -571,6 +600,7 @@ def run_ours(args, rank, world, local_rank):
                    f"({N_COPIES * 2 * B * H * L * d * 2 / 2**20:.0f} MiB of K/V > L2)"},
         "decode_tok_s": B * world / (stage_ms["decode"] * 1e-3),
         "full_cache_decode": full_cache,
+        "hit_rate": hit,
         "hbm_gbs_algorithmic_step": alg["step"] * heads / (ms_per_step * 1e-3) / 1e9,
         "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
         "stage_ms_note": stage_method + ("; the vote runs inside the score kernel" if vote_fused else "") +

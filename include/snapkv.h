@@ -217,6 +217,31 @@ SNAPKV_API snapkv_status snapkv_decode_attend_noalloc(const void* q, const void*
                                                       int32_t heads, int32_t head_dim, int32_t dtype,
                                                       int32_t* dev_status, snapkv_stream_t stream);
 
+/*
+ * snapkv_hit_rate — the explainer's Hit Rate diagnostic ([SnapKV] Hit Rate（適中率）の定式化):
+ * how much of a generation-time query's attention the kept positions cover. For every sequence b
+ * and head h, A_cur = softmax(q . K_cache[r]^T / sqrt(d), r < len[b]) ([KVcache] 22.2, the
+ * uncompressed cache) taken at the prefix positions j < l_prefix; then
+ *   total[b,h] = #{ j : A_cur[j] > theta }                (sum of M_threshold)
+ *   hits[b,h]  = #{ j in idx[b,h] : A_cur[j] > theta }    (sum of O = M_threshold AND M_vote)
+ * and the hit rate is H = sum(hits) / sum(total) (the explainer uses theta = 0.05). The threshold
+ * test runs in fp32 on the GPU, so a weight within a few ulps of theta may land on either side.
+ *
+ * q           device [B, H, d], the query of a decode step
+ * k_cache     device [B, H, cap, d], the uncompressed cache (prompt rows first)
+ * len         device int32 [B], cached rows (clamped to cap, reported as SNAPKV_ERR_CAPACITY)
+ * l_prefix    prefix length, 1 <= l_prefix <= min(cap, 2^20)
+ * idx         device int32 [B, H, k], the kept prefix positions (an index outside [0, l_prefix) is
+ *             skipped and reported as SNAPKV_ERR_INVALID_ARG in *dev_status); k >= 0
+ * theta       >= 0
+ * hits, total device int32 [B, H]
+ */
+SNAPKV_API snapkv_status snapkv_hit_rate(const void* q, const void* k_cache, int64_t cap, const int32_t* len,
+                                         int64_t l_prefix, const int32_t* idx, int64_t k, int32_t batch,
+                                         int32_t heads, int32_t head_dim, int32_t dtype, double theta,
+                                         int32_t* hits, int32_t* total, int32_t* dev_status,
+                                         snapkv_stream_t stream);
+
 /* Human-readable name of a status value (a static string; bits are listed when several). */
 SNAPKV_API const char* snapkv_status_string(int32_t status);
 

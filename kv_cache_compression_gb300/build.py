@@ -9,7 +9,7 @@ from concurrent.futures import ThreadPoolExecutor
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _CSRC = os.path.join(_HERE, "csrc")
 _BUILD = os.path.join(_HERE, "_build")
-SOURCES = ["abi.cu", "vote_simt.cu", "vote_tc.cu", "vote_cluster.cu", "pool_topk.cu", "gather.cu", "decode.cu"]
+SOURCES = ["abi.cu", "vote_simt.cu", "vote_tc.cu", "vote_cluster.cu", "pool_topk.cu", "gather.cu", "decode.cu", "hit_rate.cu"]
 HEADERS = ["snapkv_common.cuh", "snapkv_internal.h", "sm100_ptx.cuh", "tc_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

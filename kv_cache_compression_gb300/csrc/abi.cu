@@ -307,4 +307,39 @@ snapkv_status snapkv_decode_attend_noalloc(const void* q, const void* k_cache, c
   return SNAPKV_OK;
 }
 
+snapkv_status snapkv_hit_rate(const void* q, const void* k_cache, int64_t cap, const int32_t* len, int64_t l_prefix,
+                              const int32_t* idx, int64_t k, int32_t batch, int32_t heads, int32_t head_dim,
+                              int32_t dtype, double theta, int32_t* hits, int32_t* total, int32_t* dev_status,
+                              snapkv_stream_t stream) {
+  if (!q || !k_cache || !len || !hits || !total || (k > 0 && !idx)) return SNAPKV_ERR_INVALID_ARG;
+  if (batch < 1 || heads < 1 || cap < 1 || cap > kMaxPrompt || k < 0) return SNAPKV_ERR_INVALID_ARG;
+  if ((int64_t)batch * heads > 2147483647LL) return SNAPKV_ERR_INVALID_ARG;
+  if (l_prefix < 1 || l_prefix > cap || l_prefix > ((int64_t)1 << 20)) return SNAPKV_ERR_INVALID_ARG;
+  if (!(theta >= 0.0)) return SNAPKV_ERR_INVALID_ARG;
+  if (dtype != SNAPKV_F32 && dtype != SNAPKV_BF16) return SNAPKV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return SNAPKV_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || ((uintptr_t)len & 3u) || ((uintptr_t)idx & 3u) ||
+      ((uintptr_t)hits & 3u) || ((uintptr_t)total & 3u) || ((uintptr_t)dev_status & 3u))
+    return SNAPKV_ERR_INVALID_ARG;
+  HitRateJob job;
+  job.batch = batch;
+  job.heads = heads;
+  job.head_dim = head_dim;
+  job.dtype = dtype;
+  job.cap = cap;
+  job.l_prefix = l_prefix;
+  job.k_sel = k;
+  job.theta = theta;
+  job.q = q;
+  job.k_cache = k_cache;
+  job.len = len;
+  job.idx = idx;
+  job.hits = hits;
+  job.total = total;
+  job.dev_status = dev_status;
+  job.stream = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_hit_rate(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  return SNAPKV_OK;
+}
+
 }  // extern "C"

@@ -94,6 +94,23 @@ cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, v
                           int32_t* dev_status, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeJob& job);
 
+// One hit-rate diagnostic call, after host-side validation.
+struct HitRateJob {
+  int batch, heads, head_dim, dtype;
+  int64_t cap, l_prefix, k_sel;
+  double theta;
+  const void* q;
+  const void* k_cache;
+  const int32_t* len;
+  const int32_t* idx;
+  int32_t* hits;
+  int32_t* total;
+  int32_t* dev_status;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_hit_rate(const HitRateJob& job);
+
 // Size of the built-in scratch array behind snapkv_decode_attend_noalloc.
 constexpr size_t kDecodeNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB
 // Decode attention with the split partials and tickets in the built-in scratch array

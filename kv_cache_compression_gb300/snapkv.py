@@ -76,6 +76,8 @@ def lib():
         L.snapkv_decode_attend.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, P, SZ, P, P]
         L.snapkv_decode_attend_noalloc.restype = I32
         L.snapkv_decode_attend_noalloc.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, P, P]
+        L.snapkv_hit_rate.restype = I32
+        L.snapkv_hit_rate.argtypes = [P, P, I64, P, I64, P, I64, I32, I32, I32, I32, ctypes.c_double, P, P, P, P]
         L.snapkv_status_string.restype = ctypes.c_char_p
         L.snapkv_status_string.argtypes = [I32]
         L.snapkv_abi_version.restype = I32
@@ -190,6 +192,23 @@ def append(k_new, v_new, k_cache, v_cache, len_, *, dev_status=None, stream=None
                              d, _dtype_code(k_cache), _ptr(dev_status), _stream_handle(stream))
     if st != OK:
         raise SnapKVError(st, "snapkv_append")
+
+
+def hit_rate(q, k_cache, len_, idx, l_prefix, *, theta=0.05, dev_status=None, stream=None):
+    """snapkv_hit_rate: per (sequence, head) counts (hits, total) of the explainer's hit rate, for
+    the query q [B,H,d] over the uncompressed cache k_cache [B,H,cap,d] (len rows) and the kept
+    prefix positions idx [B,H,k]. H = hits.sum() / total.sum()."""
+    import torch
+    B, H, cap, d = k_cache.shape
+    hits = torch.empty((B, H), dtype=torch.int32, device=k_cache.device)
+    total = torch.empty((B, H), dtype=torch.int32, device=k_cache.device)
+    k = int(idx.shape[-1])
+    st = lib().snapkv_hit_rate(_ptr(q), _ptr(k_cache), int(cap), _ptr(len_), int(l_prefix), _ptr(idx), k, B, H, d,
+                               _dtype_code(k_cache), float(theta), _ptr(hits), _ptr(total), _ptr(dev_status),
+                               _stream_handle(stream))
+    if st != OK:
+        raise SnapKVError(st, "snapkv_hit_rate")
+    return hits, total
 
 
 def decode_attend(q, k_cache, v_cache, len_, *, out=None, workspace=None, dev_status=None, stream=None):

@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = sk.declared_functions()
-    assert len(names) == 10
+    assert len(names) == 11
     for n in names:
         assert hasattr(lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", sk.library_path()], capture_output=True, text=True).stdout
@@ -99,6 +99,25 @@ def test_decode_and_append_reject_bad_arguments(lib):
         == sk.ERR_WORKSPACE
     assert lib.snapkv_decode_attend(P(16), P(32), P(48), 10, P(64), P(88), 1, 1, 64, 0, P(256), 1 << 20, None,
                                     None) == sk.ERR_INVALID_ARG               # misaligned output
+
+
+def test_hit_rate_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p
+    ok = dict(q=P(16), k=P(32), cap=100, len_=P(48), l_prefix=90, idx=P(64), k_sel=10, B=1, H=2, d=128, dt=1,
+              theta=0.05, hits=P(80), total=P(96))
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return lib.snapkv_hit_rate(a["q"], a["k"], a["cap"], a["len_"], a["l_prefix"], a["idx"], a["k_sel"], a["B"],
+                                   a["H"], a["d"], a["dt"], a["theta"], a["hits"], a["total"], None, None)
+    assert call(q=None) == sk.ERR_INVALID_ARG
+    assert call(l_prefix=0) == sk.ERR_INVALID_ARG
+    assert call(l_prefix=101) == sk.ERR_INVALID_ARG           # beyond the cache
+    assert call(theta=-0.1) == sk.ERR_INVALID_ARG
+    assert call(theta=float("nan")) == sk.ERR_INVALID_ARG
+    assert call(idx=None) == sk.ERR_INVALID_ARG                # k > 0 needs indices
+    assert call(d=96) == sk.ERR_UNSUPPORTED
+    assert call(q=P(24)) == sk.ERR_INVALID_ARG                 # misaligned
 
 
 def test_status_strings(lib):

@@ -206,6 +206,28 @@ def compress_head(q_obs: np.ndarray, k: np.ndarray, v: np.ndarray, *, pool_kerne
                       v_c=gather_with_window(v, idx, l_prefix))
 
 
+def compress_kv_head_gqa(q_obs_group: np.ndarray, k: np.ndarray, v: np.ndarray, *, pool_kernel: int,
+                         ratio_p: float = 0.0, budget: int = 0, scope: str = PROMPT_CAUSAL) -> Compressed:
+    """SnapKV compression of one KV head shared by G query heads (grouped-query attention).
+
+    The pages are silent on grouped heads; the reading taken: every query head of the group votes
+    with its own row softmax over the shared keys, the KV head's vote is the sum of the G votes,
+    and pooling, selection and gather then run once on the KV head as for a single head.
+    q_obs_group: [G, L_obs, d] window queries of the group; k, v: the KV head's prompt [L_prompt, d].
+    """
+    l_obs = q_obs_group.shape[1]
+    l_prefix = prefix_length(k.shape[0], l_obs)
+    k_sel = kept_slots(l_prefix, ratio_p, budget)
+    c = np.zeros(l_prefix)
+    for g in range(q_obs_group.shape[0]):
+        c = c + vote(q_obs_group[g], k, scope)
+    p = max_pool(c, pool_kernel)
+    idx = select_topk(p, k_sel)
+    tau = kth_largest(p, k_sel) if k_sel > 0 else float("nan")
+    return Compressed(c=c, p=p, idx=idx, tau=tau, k_c=gather_with_window(k, idx, l_prefix),
+                      v_c=gather_with_window(v, idx, l_prefix))
+
+
 def append(k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray, v_new: np.ndarray):
     """[KVcache] 22.2: K_cache <- [K_cache; k_t], V_cache <- [V_cache; v_t]."""
     return (np.concatenate([k_cache, np.asarray(k_new)[None, :]], axis=0),

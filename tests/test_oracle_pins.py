@@ -424,3 +424,37 @@ def test_hit_count_dominant_key_and_prefix_restriction():
         kk[jstar, 0] = 5.0
         h = orc.hit_count(q, kk, l_prefix, np.array(kept), theta=0.05)
         assert (h.hits, h.total) == want, (jstar, kept)
+
+
+# ------------------------------------------------------------------------------------------------
+# Grouped-query attention (the KV head's vote sums its query heads' votes)
+# ------------------------------------------------------------------------------------------------
+
+def test_gqa_single_query_head_is_plain_compression():
+    rng = np.random.default_rng(51)
+    q, k, v = _rand(rng, 8, 16), _rand(rng, 100, 16), _rand(rng, 100, 16)
+    a = orc.compress_kv_head_gqa(q[None], k, v, pool_kernel=5, budget=20)
+    b = orc.compress_head(q, k, v, pool_kernel=5, budget=20)
+    assert np.array_equal(a.idx, b.idx) and np.allclose(a.c, b.c, rtol=0, atol=0)
+
+
+def test_gqa_identical_query_heads_scale_the_vote():
+    """G copies of one query head: the vote is exactly G times the single head's (a sum of equal
+    terms), so pooling and selection are unchanged."""
+    rng = np.random.default_rng(52)
+    q, k, v = _rand(rng, 8, 16), _rand(rng, 120, 16), _rand(rng, 120, 16)
+    one = orc.compress_head(q, k, v, pool_kernel=7, budget=30)
+    four = orc.compress_kv_head_gqa(np.stack([q] * 4), k, v, pool_kernel=7, budget=30)
+    assert np.allclose(four.c, 4 * one.c, rtol=1e-15, atol=0)
+    assert np.array_equal(four.idx, one.idx)
+
+
+def test_gqa_vote_sum_over_prompt_is_group_times_window():
+    """Each query head's rows sum to one over the keys they see, so the group's votes over every
+    prompt column sum to G * L_obs (and the prefix columns alone carry less)."""
+    rng = np.random.default_rng(53)
+    qg, k = _rand(rng, 3, 8, 16, scale=2.0), _rand(rng, 90, 16)
+    tot = sum(orc.vote_all_columns(qg[g], k).sum() for g in range(3))
+    assert abs(tot - 24.0) < 1e-12
+    gq = orc.compress_kv_head_gqa(qg, k, k, pool_kernel=3, budget=10)
+    assert gq.c.sum() < 24.0

@@ -157,6 +157,27 @@ SNAPKV_API snapkv_status snapkv_compress_profiled(const snapkv_compress_params* 
                                                   void* const* stage_events, int32_t n_events);
 
 /*
+ * snapkv_compress_gqa — snapkv_compress for grouped-query attention: `q_heads` query heads share
+ * the params' `heads` KV heads (q_heads a multiple of heads; the G = q_heads / heads query heads of
+ * KV head h are h*G .. h*G + G - 1). The pages do not cover grouped heads; the reading taken: each
+ * query head votes with its own row softmax over its KV head's keys ([SnapKV] 投票メカニズム), the
+ * KV head's vote is the sum of its G query heads' votes, and pooling, selection and gather run per
+ * KV head. G * L_obs <= 128 (else SNAPKV_ERR_UNSUPPORTED).
+ *
+ * q_obs     device [B, q_heads, L_obs, d]
+ * k, v      device [B, heads, L_prompt, d]
+ * vote_out  device fp32 [B, heads, L_prefix] (the summed vote; NULL: not returned)
+ * every other argument as for snapkv_compress, with heads = KV heads; the workspace size is
+ * snapkv_compress_gqa_workspace_size(params, q_heads).
+ */
+SNAPKV_API size_t snapkv_compress_gqa_workspace_size(const snapkv_compress_params* params, int32_t q_heads);
+SNAPKV_API snapkv_status snapkv_compress_gqa(const snapkv_compress_params* params, int32_t q_heads,
+                                             const void* q_obs, const void* k, const void* v, void* k_out,
+                                             void* v_out, int64_t cap, int32_t* len_out, int32_t* idx_out,
+                                             float* vote_out, void* workspace, size_t workspace_bytes,
+                                             int32_t* dev_status, snapkv_stream_t stream);
+
+/*
  * snapkv_append — one decode step's cache append ([KVcache] 22.2): for every sequence b and
  * head h, row len[b] of k_cache / v_cache receives k_new / v_new, then len[b] += 1.
  *

@@ -24,9 +24,12 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
   return a0 < b0 + bn && b0 < a0 + an;
 }
 
-// Validates the problem statement; on success fills l_prefix and k_sel.
-snapkv_status check_params(const snapkv_compress_params* p, int64_t* l_prefix, int64_t* k_sel) {
+// Validates the problem statement (q_heads query heads share the params' KV heads); on success
+// fills l_prefix, k_sel and the window-query rows per KV head.
+snapkv_status check_params(const snapkv_compress_params* p, int32_t q_heads, int64_t* l_prefix, int64_t* k_sel,
+                           int* q_rows) {
   if (!p) return SNAPKV_ERR_INVALID_ARG;
+  if (q_heads < p->heads || p->heads < 1 || q_heads % p->heads != 0) return SNAPKV_ERR_INVALID_ARG;
   if (p->batch < 1 || p->heads < 1 || p->head_dim < 1 || p->l_obs < 1 || p->pool_kernel < 1)
     return SNAPKV_ERR_INVALID_ARG;
   if (p->l_prompt <= p->l_obs || p->l_prompt > kMaxPrompt) return SNAPKV_ERR_INVALID_ARG;
@@ -39,7 +42,7 @@ snapkv_status check_params(const snapkv_compress_params* p, int64_t* l_prefix, i
   if ((int64_t)p->batch * p->heads > 65535) return SNAPKV_ERR_INVALID_ARG;  // grid.y limit
   if (p->head_dim != 64 && p->head_dim != 128) return SNAPKV_ERR_UNSUPPORTED;
   if (p->pool_kernel % 2 == 0) return SNAPKV_ERR_UNSUPPORTED;
-  if (p->l_obs > kMaxObs) return SNAPKV_ERR_UNSUPPORTED;
+  if (p->l_obs > kMaxObs || (int64_t)(q_heads / p->heads) * p->l_obs > kMaxObs) return SNAPKV_ERR_UNSUPPORTED;
   const int64_t lp = p->l_prompt - p->l_obs;
   int64_t k;
   if (p->budget > 0)
@@ -50,26 +53,28 @@ snapkv_status check_params(const snapkv_compress_params* p, int64_t* l_prefix, i
   if (k > lp) k = lp;
   *l_prefix = lp;
   *k_sel = k;
+  *q_rows = (q_heads / p->heads) * p->l_obs;
   return SNAPKV_OK;
 }
 
 }  // namespace
 
-CompressLayout compress_layout(int batch, int heads, int l_obs, int64_t l_prompt, int64_t k_sel) {
+CompressLayout compress_layout(int batch, int heads, int l_obs, int q_rows, int64_t l_prompt, int64_t k_sel) {
   CompressLayout L;
   const size_t bh = (size_t)batch * heads;
   const int64_t l_prefix = l_prompt - l_obs;
   L.vote_chunk = kVoteChunk;
   L.n_chunk_all = (int)((l_prompt + kVoteChunk - 1) / kVoteChunk);
   L.n_chunk_prefix = (int)((l_prefix + kVoteChunk - 1) / kVoteChunk);
-  const int64_t tc_items = (l_prompt + vote_tc_keys_per_item(l_obs) - 1) / vote_tc_keys_per_item(l_obs);
+  const int64_t kpi = vote_tc_keys_per_item(q_rows, l_obs);
+  const int64_t tc_items = (l_prompt + kpi - 1) / kpi;
   const int64_t chunks = tc_items > L.n_chunk_all ? tc_items : L.n_chunk_all;
   L.partial = 0;
-  L.c = up256(bh * chunks * l_obs * 2 * sizeof(float));
+  L.c = up256(bh * chunks * q_rows * 2 * sizeof(float));
   L.p = L.c + up256(bh * l_prefix * sizeof(float));
   L.idx = L.p + up256(bh * l_prefix * sizeof(float));
   L.tc_zsum = L.idx + up256(bh * (k_sel > 0 ? k_sel : 1) * sizeof(int32_t));
-  L.tc_counters = L.tc_zsum + up256(bh * l_obs * sizeof(double));
+  L.tc_counters = L.tc_zsum + up256(bh * q_rows * sizeof(double));
   L.total = L.tc_counters + up256(bh * sizeof(uint32_t));
   return L;
 }
@@ -107,24 +112,34 @@ const char* snapkv_status_string(int32_t status) {
 
 int64_t snapkv_compress_kept(const snapkv_compress_params* params) {
   int64_t lp = 0, k = 0;
-  if (check_params(params, &lp, &k) != SNAPKV_OK) return -1;
+  int rows = 0;
+  if (!params || check_params(params, params->heads, &lp, &k, &rows) != SNAPKV_OK) return -1;
   return k;
 }
 
-size_t snapkv_compress_workspace_size(const snapkv_compress_params* params) {
+size_t snapkv_compress_gqa_workspace_size(const snapkv_compress_params* params, int32_t q_heads) {
   int64_t lp = 0, k = 0;
-  if (check_params(params, &lp, &k) != SNAPKV_OK) return 0;
-  return compress_layout(params->batch, params->heads, params->l_obs, params->l_prompt, k).total;
+  int rows = 0;
+  if (!params || check_params(params, q_heads, &lp, &k, &rows) != SNAPKV_OK) return 0;
+  return compress_layout(params->batch, params->heads, params->l_obs, rows, params->l_prompt, k).total;
 }
 
-snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, const void* q_obs, const void* k,
-                                       const void* v, void* k_out, void* v_out, int64_t cap, int32_t* len_out,
-                                       int32_t* idx_out, float* vote_out, void* workspace, size_t workspace_bytes,
-                                       int32_t* dev_status, snapkv_stream_t stream, void* const* stage_events,
-                                       int32_t n_events) {
+size_t snapkv_compress_workspace_size(const snapkv_compress_params* params) {
+  return params ? snapkv_compress_gqa_workspace_size(params, params->heads) : 0;
+}
+
+}  // extern "C"
+
+namespace {
+
+snapkv_status compress_impl(const snapkv_compress_params* params, int32_t q_heads, const void* q_obs, const void* k,
+                            const void* v, void* k_out, void* v_out, int64_t cap, int32_t* len_out, int32_t* idx_out,
+                            float* vote_out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            snapkv_stream_t stream, void* const* stage_events, int32_t n_events) {
   if (n_events < 0 || (n_events > 0 && !stage_events)) return SNAPKV_ERR_INVALID_ARG;
   int64_t l_prefix = 0, k_sel = 0;
-  const snapkv_status st = check_params(params, &l_prefix, &k_sel);
+  int q_rows = 0;
+  const snapkv_status st = check_params(params, q_heads, &l_prefix, &k_sel, &q_rows);
   if (st != SNAPKV_OK) return st;
   if (!q_obs || !k || !v || !k_out || !v_out || !len_out) return SNAPKV_ERR_INVALID_ARG;
   if (!aligned16(q_obs) || !aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out))
@@ -133,7 +148,8 @@ snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, con
       ((uintptr_t)dev_status & 3u))
     return SNAPKV_ERR_INVALID_ARG;
   if (cap < k_sel + params->l_obs || cap > kMaxPrompt) return SNAPKV_ERR_CAPACITY;
-  const CompressLayout L = compress_layout(params->batch, params->heads, params->l_obs, params->l_prompt, k_sel);
+  const CompressLayout L =
+      compress_layout(params->batch, params->heads, params->l_obs, q_rows, params->l_prompt, k_sel);
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SNAPKV_ERR_WORKSPACE;
 
   const size_t esize = params->dtype == SNAPKV_BF16 ? 2 : 4;
@@ -151,6 +167,7 @@ snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, con
   job.heads = params->heads;
   job.head_dim = params->head_dim;
   job.l_obs = params->l_obs;
+  job.q_rows = q_rows;
   job.pool_kernel = params->pool_kernel;
   job.scope = params->softmax_scope;
   job.dtype = params->dtype;
@@ -204,6 +221,28 @@ snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, con
     return SNAPKV_ERR_CUDA;
   }
   return SNAPKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, const void* q_obs, const void* k,
+                                       const void* v, void* k_out, void* v_out, int64_t cap, int32_t* len_out,
+                                       int32_t* idx_out, float* vote_out, void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_status, snapkv_stream_t stream, void* const* stage_events,
+                                       int32_t n_events) {
+  if (!params) return SNAPKV_ERR_INVALID_ARG;
+  return compress_impl(params, params->heads, q_obs, k, v, k_out, v_out, cap, len_out, idx_out, vote_out, workspace,
+                       workspace_bytes, dev_status, stream, stage_events, n_events);
+}
+
+snapkv_status snapkv_compress_gqa(const snapkv_compress_params* params, int32_t q_heads, const void* q_obs,
+                                  const void* k, const void* v, void* k_out, void* v_out, int64_t cap,
+                                  int32_t* len_out, int32_t* idx_out, float* vote_out, void* workspace,
+                                  size_t workspace_bytes, int32_t* dev_status, snapkv_stream_t stream) {
+  return compress_impl(params, q_heads, q_obs, k, v, k_out, v_out, cap, len_out, idx_out, vote_out, workspace,
+                       workspace_bytes, dev_status, stream, nullptr, 0);
 }
 
 snapkv_status snapkv_compress(const snapkv_compress_params* params, const void* q_obs, const void* k,

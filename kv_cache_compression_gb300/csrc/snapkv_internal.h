@@ -10,6 +10,7 @@ namespace snapkv {
 // One compression call, after host-side validation.
 struct CompressJob {
   int batch, heads, head_dim, l_obs, pool_kernel, scope, dtype;
+  int q_rows;          // window-query rows per KV head: (query heads / KV heads) * l_obs
   int64_t l_prompt, l_prefix, k_sel, cap;
   const void* q_obs;
   const void* k;
@@ -52,7 +53,7 @@ struct CompressLayout {
   int vote_chunk, n_chunk_all, n_chunk_prefix;
 };
 
-CompressLayout compress_layout(int batch, int heads, int l_obs, int64_t l_prompt, int64_t k_sel);
+CompressLayout compress_layout(int batch, int heads, int l_obs, int q_rows, int64_t l_prompt, int64_t k_sel);
 
 cudaError_t launch_vote_simt(const CompressJob& job);
 // Tensor-core score + vote (bf16, d 64/128, L_obs <= 64, items per head <= 2 x SMs).
@@ -60,7 +61,7 @@ bool vote_tc_eligible(const CompressJob& job);
 // The cluster-per-head tensor-core kernel (a head's keys fit 8 CTAs x 4 TMEM slots).
 bool vote_cluster_eligible(const CompressJob& job);
 cudaError_t launch_vote_cluster(const CompressJob& job);
-int vote_tc_keys_per_item(int l_obs);
+int vote_tc_keys_per_item(int q_rows, int l_obs);
 cudaError_t launch_vote_tc(const CompressJob& job);
 // Max-pool + top-k; for prefixes the cluster kernel handles it also writes K_c, V_c and len_out
 // (*gathered = true), otherwise launch_gather must follow.

@@ -1,5 +1,7 @@
-// Score + softmax + vote with one thread-block cluster per head (bf16, d = 64 or 128, L_obs <= 64,
-// prompts of at most 8 CTAs x 4 TMEM slots of keys: 16K keys at L_obs 32).
+// Score + softmax + vote with one thread-block cluster per head (bf16, d = 64 or 128, at most 128
+// window-query rows per head, prompts of at most 8 CTAs x 4 TMEM slots of keys: 16K keys at 32
+// rows). Under grouped-query attention a KV head's rows are its query heads' windows one after
+// another (row i at window position i mod L_obs), and the vote sums every row.
 //
 // SnapKV explainer ("論文解説: SnapKV"), sections 投票メカニズム and アルゴリズム: logits
 // s_ij = q_i . k_j / sqrt(d) of the L_obs window queries against every prompt key, the row
@@ -47,7 +49,7 @@ constexpr long long kDrainLimit = 400000000LL;
 
 struct ClArgs {
   int64_t l_prompt, l_prefix;
-  int l_obs, scope, n_items, keys_per_item, csize;
+  int l_obs, rows, scope, n_items, keys_per_item, csize;   // rows: window-query rows per head
   float scale_log2;
   float* c_out;       // [BH][l_prefix]
   int32_t* dev_status;
@@ -79,7 +81,7 @@ struct ClLayout {
   static constexpr int BYTES_USED = OFF_MISC + 64 + 1024;
   static constexpr int BYTES = BYTES_USED > 120 * 1024 ? BYTES_USED : 120 * 1024;
   static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, N);
-  static_assert(N % 16 == 0 && N >= 16 && N <= 64, "N");
+  static_assert(N % 16 == 0 && N >= 16 && N <= 128, "N");
   static_assert(kItemsPerCta * TI * N == (int)kTmemCols, "four slots fill TMEM");
   static_assert(QB_BYTES % 1024 == 0 && OFF_Q % 1024 == 0, "swizzle atoms");
   static_assert(STAGES >= 2 && BYTES <= 232448, "shared memory");
@@ -91,7 +93,9 @@ __device__ __forceinline__ int item_tiles(const ClArgs& a, int item, int TI) {
   return t < TI ? t : TI;
 }
 
-template <int D, int N>
+// GQ: grouped-query rows, whose window position row mod L_obs comes from a table (a separate
+// instantiation, so that the single-head case keeps its simpler epilogue).
+template <int D, int N, bool GQ>
 __global__ void __launch_bounds__(kThreadsCl, 1)
 vote_cluster_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                     ClArgs a) {
@@ -112,6 +116,7 @@ vote_cluster_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   float* rowstat = reinterpret_cast<float*>(base + Lay::OFF_ROWSTAT);
   float* cvrow = reinterpret_cast<float*>(base + Lay::OFF_CV);
   __shared__ int no_abort;
+  __shared__ int row_pos[GQ ? N : 1];   // window position of each query row (row mod L_obs)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ptx::cluster_rank();
@@ -129,6 +134,8 @@ vote_cluster_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     ptx::tmem_alloc(&misc[0], kTmemCols);
     ptx::tmem_relinquish();
   }
+  if (GQ)
+    for (int i = threadIdx.x; i < N; i += kThreadsCl) row_pos[i] = i % a.l_obs;
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -232,8 +239,8 @@ vote_cluster_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     ptx::tmem_wait_ld();
   };
   auto visible = [&](int row, int64_t key) {
-    return row < a.l_obs && key < a.l_prompt &&
-           (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + row : key <= lim);
+    return row < a.rows && key < a.l_prompt &&
+           (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + (GQ ? row_pos[row] : row) : key <= lim);
   };
 
   if (epi) {
@@ -330,7 +337,7 @@ vote_cluster_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           Z = fmaf(__uint_as_float(ptx::dsmem_ld_u32(ptx::map_rank(&rowstat[N + etid], (uint32_t)r))),
                    ex2(mr[r] - M), Z);
       // rows past L_obs (zero logits) and rows with no visible key get zero weight
-      cvrow[etid] = (etid < a.l_obs && Z > 0.f) ? M + log2f(Z) : INFINITY;
+      cvrow[etid] = (etid < a.rows && Z > 0.f) ? M + log2f(Z) : INFINITY;
     }
   }
   __syncwarp();
@@ -371,13 +378,13 @@ vote_cluster_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   ptx::cluster_wait();   // no CTA leaves while its peers may still read its (M, Z)
 }
 
-template <int D, int N>
+template <int D, int N, bool GQ>
 int cluster_smem_ready() {
   // The shared-memory attribute is set once per instantiation (0 unknown, 1 set, -1 failed).
   static std::atomic<int> state{0};
   int st = state.load(std::memory_order_acquire);
   if (st == 0) {
-    st = cudaFuncSetAttribute(vote_cluster_kernel<D, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    st = cudaFuncSetAttribute(vote_cluster_kernel<D, N, GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               ClLayout<D, N>::BYTES) == cudaSuccess
              ? 1
              : -1;
@@ -386,26 +393,32 @@ int cluster_smem_ready() {
   return st;
 }
 
-int n_pad(int l_obs) { return l_obs <= 16 ? 16 : (l_obs <= 32 ? 32 : 64); }
+// Padded row count: 16, 32, 64 or 128 for one head's window, 64 or 128 for grouped windows.
+int n_pad(int rows, int l_obs) {
+  const int n = rows <= 16 ? 16 : (rows <= 32 ? 32 : (rows <= 64 ? 64 : 128));
+  return (rows != l_obs && n < 64) ? 64 : n;
+}
 
 int cluster_ctas(const CompressJob& job) {
-  const int kpi = (128 / n_pad(job.l_obs)) * kTileKeys;
+  const int kpi = (128 / n_pad(job.q_rows, job.l_obs)) * kTileKeys;
   const int64_t items = (job.l_prompt + kpi - 1) / kpi;
   return (int)((items + kItemsPerCta - 1) / kItemsPerCta);
 }
 
-template <int D, int N>
+template <int D, int N, bool GQ>
 cudaError_t launch_cluster_typed(const CompressJob& job) {
   using Lay = ClLayout<D, N>;
-  if (cluster_smem_ready<D, N>() < 0) return cudaErrorInvalidConfiguration;
+  if (cluster_smem_ready<D, N, GQ>() < 0) return cudaErrorInvalidConfiguration;
   CUtensorMap mk, mq;
   const int64_t bh = (int64_t)job.batch * job.heads;
-  if (!tc::make_map(&mk, job.k, D, job.l_prompt, bh, kTileKeys) || !tc::make_map(&mq, job.q_obs, D, job.l_obs, bh, N))
+  if (!tc::make_map(&mk, job.k, D, job.l_prompt, bh, kTileKeys) ||
+      !tc::make_map(&mq, job.q_obs, D, job.q_rows, bh, N))
     return cudaErrorInvalidValue;
   ClArgs a;
   a.l_prompt = job.l_prompt;
   a.l_prefix = job.l_prefix;
   a.l_obs = job.l_obs;
+  a.rows = job.q_rows;
   a.scope = job.scope;
   a.keys_per_item = Lay::TI * kTileKeys;
   a.n_items = (int)((job.l_prompt + a.keys_per_item - 1) / a.keys_per_item);
@@ -426,7 +439,7 @@ cudaError_t launch_cluster_typed(const CompressJob& job) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   job.mark(2 * kStageScore);
-  const cudaError_t err = cudaLaunchKernelEx(&cfg, vote_cluster_kernel<D, N>, mk, mq, a);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, vote_cluster_kernel<D, N, GQ>, mk, mq, a);
   job.mark(2 * kStageScore + 1);
   job.mark(2 * kStageVote);
   job.mark(2 * kStageVote + 1);
@@ -436,22 +449,28 @@ cudaError_t launch_cluster_typed(const CompressJob& job) {
 }  // namespace
 
 bool vote_cluster_eligible(const CompressJob& job) {
-  if (job.dtype != SNAPKV_BF16 || job.l_obs > 64) return false;
+  if (job.dtype != SNAPKV_BF16 || job.q_rows > 128) return false;
   if (job.head_dim != 64 && job.head_dim != 128) return false;
   const int c = cluster_ctas(job);
   return c >= 1 && c <= kMaxCtas && (int64_t)job.batch * job.heads * c < ((int64_t)1 << 31);
 }
 
 cudaError_t launch_vote_cluster(const CompressJob& job) {
-  const int n = n_pad(job.l_obs);
-  if (job.head_dim == 64) {
-    if (n == 16) return launch_cluster_typed<64, 16>(job);
-    if (n == 32) return launch_cluster_typed<64, 32>(job);
-    return launch_cluster_typed<64, 64>(job);
+  const int n = n_pad(job.q_rows, job.l_obs);
+  if (job.q_rows != job.l_obs) {
+    if (job.head_dim == 64) return n == 64 ? launch_cluster_typed<64, 64, true>(job) : launch_cluster_typed<64, 128, true>(job);
+    return n == 64 ? launch_cluster_typed<128, 64, true>(job) : launch_cluster_typed<128, 128, true>(job);
   }
-  if (n == 16) return launch_cluster_typed<128, 16>(job);
-  if (n == 32) return launch_cluster_typed<128, 32>(job);
-  return launch_cluster_typed<128, 64>(job);
+  if (job.head_dim == 64) {
+    if (n == 16) return launch_cluster_typed<64, 16, false>(job);
+    if (n == 32) return launch_cluster_typed<64, 32, false>(job);
+    if (n == 64) return launch_cluster_typed<64, 64, false>(job);
+    return launch_cluster_typed<64, 128, false>(job);
+  }
+  if (n == 16) return launch_cluster_typed<128, 16, false>(job);
+  if (n == 32) return launch_cluster_typed<128, 32, false>(job);
+  if (n == 64) return launch_cluster_typed<128, 64, false>(job);
+  return launch_cluster_typed<128, 128, false>(job);
 }
 
 }  // namespace snapkv

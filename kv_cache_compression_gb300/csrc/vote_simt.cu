@@ -8,7 +8,9 @@
 // (head, chunk of columns, window row), the partial row maximum and partial sum of exponentials.
 // Pass 1 (vote) merges those partials into m_i and 1/Z_i, recomputes the logits of the prefix
 // columns and writes C_j. Logits live in the log2 domain (scaled by log2(e)/sqrt(d)) so every
-// exponential is one ex2.
+// exponential is one ex2. Under grouped-query attention a KV head's window rows are its query
+// heads' rows one after another (rows = G * L_obs); row i sits at window position i mod L_obs, and
+// the vote sums every row.
 #include "snapkv_common.cuh"
 #include "snapkv_internal.h"
 
@@ -22,10 +24,10 @@ constexpr int kGroups = kThreads / kTile;   // window rows are split over 4 grou
 struct VoteParams {
   const void* q_obs;
   const void* k;
-  float* partial;       // [B*H][n_chunk_all][l_obs][2] (m, z)
+  float* partial;       // [B*H][n_chunk_all][rows][2] (m, z)
   float* c_out;         // [B*H][l_prefix]
   int64_t l_prompt, l_prefix;
-  int l_obs, scope, chunk, n_chunk_all;
+  int l_obs, rows, scope, chunk, n_chunk_all;   // rows: window-query rows per head
   float scale_log2;     // log2(e) / sqrt(d)
 };
 
@@ -48,17 +50,19 @@ __global__ void __launch_bounds__(kThreads) vote_simt_kernel(VoteParams a, int p
   float* red = st_zi + LQ;                 // [kGroups][kTile] partial votes (pass 1)
   float* wred = red + kGroups * kTile;     // [warps][QG][2] warp statistics (pass 0)
 
+  __shared__ int row_pos[LQ];   // window position of each query row (row mod L_obs)
   const int tid = threadIdx.x;
   const int64_t bh = blockIdx.y;
   const int64_t col0 = (int64_t)blockIdx.x * a.chunk;
   const int64_t col1 = min(col0 + (int64_t)a.chunk, pass == 0 ? a.l_prompt : a.l_prefix);
-  const T* qg = static_cast<const T*>(a.q_obs) + bh * a.l_obs * D;
+  const T* qg = static_cast<const T*>(a.q_obs) + bh * a.rows * D;
   const T* kg = static_cast<const T*>(a.k) + bh * a.l_prompt * D;
 
+  for (int i = tid; i < LQ; i += kThreads) row_pos[i] = i % a.l_obs;
   for (int u = tid; u < LQ * VPR; u += kThreads) {
     const int i = u / VPR, cv = u % VPR;
     float f[V];
-    if (i < a.l_obs) {
+    if (i < a.rows) {
       Elem<T>::widen(ld_nc_v4(qg + (int64_t)i * D + cv * V), f);
     } else {
 #pragma unroll
@@ -70,16 +74,16 @@ __global__ void __launch_bounds__(kThreads) vote_simt_kernel(VoteParams a, int p
   if (pass == 1) {
     for (int i = tid; i < LQ; i += kThreads) {
       float m = -INFINITY, z = 0.f;
-      if (i < a.l_obs) {
-        const float* pr = a.partial + (bh * a.n_chunk_all * a.l_obs + i) * 2;
-        for (int c = 0; c < a.n_chunk_all; ++c) m = fmaxf(m, pr[(int64_t)c * a.l_obs * 2]);
+      if (i < a.rows) {
+        const float* pr = a.partial + (bh * a.n_chunk_all * a.rows + i) * 2;
+        for (int c = 0; c < a.n_chunk_all; ++c) m = fmaxf(m, pr[(int64_t)c * a.rows * 2]);
         for (int c = 0; c < a.n_chunk_all; ++c) {
-          const float mc = pr[(int64_t)c * a.l_obs * 2], zc = pr[(int64_t)c * a.l_obs * 2 + 1];
+          const float mc = pr[(int64_t)c * a.rows * 2], zc = pr[(int64_t)c * a.rows * 2 + 1];
           if (mc != -INFINITY) z += zc * ex2(mc - m);
         }
       }
-      st_m[i] = (i < a.l_obs) ? m : 0.f;
-      st_zi[i] = (i < a.l_obs && z > 0.f) ? 1.f / z : 0.f;
+      st_m[i] = (i < a.rows) ? m : 0.f;
+      st_zi[i] = (i < a.rows && z > 0.f) ? 1.f / z : 0.f;
     }
   }
   __syncthreads();
@@ -128,8 +132,8 @@ __global__ void __launch_bounds__(kThreads) vote_simt_kernel(VoteParams a, int p
 #pragma unroll
       for (int r = 0; r < QG; ++r) {
         const int i = g * QG + r;
-        const bool vis = col < col1 && i < a.l_obs &&
-                         (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? col <= a.l_prefix + i : col < a.l_prefix);
+        const bool vis = col < col1 && i < a.rows &&
+                         (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? col <= a.l_prefix + row_pos[i] : col < a.l_prefix);
         if (vis) {
           const float s = acc[r] * a.scale_log2;
           if (s > m_run[r]) {
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(kThreads) vote_simt_kernel(VoteParams a, int p
 #pragma unroll
       for (int r = 0; r < QG; ++r) {
         const int i = g * QG + r;
-        if (i < a.l_obs) csum += ex2(acc[r] * a.scale_log2 - st_m[i]) * st_zi[i];
+        if (i < a.rows) csum += ex2(acc[r] * a.scale_log2 - st_m[i]) * st_zi[i];
       }
       red[g * kTile + j] = csum;
       __syncthreads();
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(kThreads) vote_simt_kernel(VoteParams a, int p
     }
     __syncthreads();
     constexpr int kWarpsPerGroup = kTile / 32;
-    for (int i = tid; i < a.l_obs; i += kThreads) {
+    for (int i = tid; i < a.rows; i += kThreads) {
       const int gg = i / QG, r = i % QG;
       float m = -INFINITY;
       for (int w = 0; w < kWarpsPerGroup; ++w) m = fmaxf(m, wred[((gg * kWarpsPerGroup + w) * QG + r) * 2]);
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) vote_simt_kernel(VoteParams a, int p
         const float mw = wred[((gg * kWarpsPerGroup + w) * QG + r) * 2];
         if (mw != -INFINITY) z += wred[((gg * kWarpsPerGroup + w) * QG + r) * 2 + 1] * ex2(mw - m);
       }
-      float* out = a.partial + ((bh * a.n_chunk_all + blockIdx.x) * a.l_obs + i) * 2;
+      float* out = a.partial + ((bh * a.n_chunk_all + blockIdx.x) * a.rows + i) * 2;
       out[0] = m;
       out[1] = z;
     }
@@ -212,9 +216,9 @@ cudaError_t launch_typed(const CompressJob& job, const VoteParams& a) {
 
 template <typename T, int D>
 cudaError_t launch_d(const CompressJob& job, const VoteParams& a) {
-  if (job.l_obs <= 4 * kGroups) return launch_typed<T, D, 4>(job, a);
-  if (job.l_obs <= 8 * kGroups) return launch_typed<T, D, 8>(job, a);
-  if (job.l_obs <= 16 * kGroups) return launch_typed<T, D, 16>(job, a);
+  if (job.q_rows <= 4 * kGroups) return launch_typed<T, D, 4>(job, a);
+  if (job.q_rows <= 8 * kGroups) return launch_typed<T, D, 8>(job, a);
+  if (job.q_rows <= 16 * kGroups) return launch_typed<T, D, 16>(job, a);
   return launch_typed<T, D, 32>(job, a);
 }
 
@@ -234,6 +238,7 @@ cudaError_t launch_vote_simt(const CompressJob& job) {
   a.l_prompt = job.l_prompt;
   a.l_prefix = job.l_prefix;
   a.l_obs = job.l_obs;
+  a.rows = job.q_rows;
   a.scope = job.scope;
   a.chunk = job.vote_chunk;
   a.n_chunk_all = job.n_chunk_all;

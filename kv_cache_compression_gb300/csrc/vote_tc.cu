@@ -1,4 +1,6 @@
-// Score + softmax + vote on the 5th-generation tensor cores (bf16, d = 64 or 128, L_obs <= 64).
+// Score + softmax + vote on the 5th-generation tensor cores (bf16, d = 64 or 128, at most 128
+// window-query rows per head: L_obs, or G * L_obs for G query heads sharing a KV head, whose rows
+// follow one another; row i sits at window position i mod L_obs and the vote sums every row).
 //
 // SnapKV explainer ("論文解説: SnapKV"), sections 投票メカニズム and アルゴリズム: logits
 // s_ij = q_i . k_j / sqrt(d) of the L_obs window queries against every prompt key, the row
@@ -57,10 +59,10 @@ constexpr long long kDrainLimit = 400000000LL;
 
 struct TcArgs {
   int64_t l_prompt, l_prefix;
-  int l_obs, scope, n_chunk, n_queue, keys_per_item, bh_total, delta;
+  int l_obs, rows, scope, n_chunk, n_queue, keys_per_item, bh_total, delta;   // rows: window-query rows
   int resident;      // 1: one item per key chunk, logits stay in TMEM from statistics to vote
   float scale_log2;
-  double* zsum;      // [BH][l_obs]: Z_i = sum_j 2^(s'_ij) over the head's visible keys (fp64)
+  double* zsum;      // [BH][rows]: Z_i = sum_j 2^(s'_ij) over the row's visible keys (fp64)
   uint32_t* cnt;     // [BH] A items whose contribution to zsum is complete
   float* c_out;      // [BH][l_prefix]
   int32_t* dev_status;
@@ -129,7 +131,7 @@ struct TcLayout {
   static constexpr int BYTES_USED = OFF_MISC + 64 + 1024;
   static constexpr int BYTES = BYTES_USED > 120 * 1024 ? BYTES_USED : 120 * 1024;
   static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, N);
-  static_assert(N % 16 == 0 && N >= 16 && N <= 64, "N");
+  static_assert(N % 16 == 0 && N >= 16 && N <= 128, "N");
   static_assert(kSlots * TI * N == (int)kTmemCols, "four slots fill TMEM");
   static_assert(QB_BYTES % 1024 == 0, "swizzle atoms");
   static_assert(STAGES >= 2 && BYTES <= 232448, "shared memory");
@@ -159,7 +161,10 @@ __device__ __forceinline__ int tiles_of(const TcArgs& a, int chunk, int TI) {
   return t < TI ? t : TI;
 }
 
-template <int D, int N>
+// GQ: the rows are several query heads' windows (grouped-query attention), so a row's window
+// position is row mod L_obs (looked up in a table); otherwise it is the row itself. The two are
+// separate instantiations: the table lookup in the window tiles slows the common case's epilogue.
+template <int D, int N, bool GQ>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q, TcArgs a) {
   using Lay = TcLayout<D, N>;
@@ -195,6 +200,9 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
   ptx::tc_fence_after();
   const uint32_t tmem_base = c.misc[0];
   __shared__ int no_abort;
+  __shared__ int row_pos[GQ ? N : 1];   // window position of each query row (row mod L_obs)
+  if (GQ)
+    for (int i = threadIdx.x; i < N; i += kThreadsTc) row_pos[i] = i % a.l_obs;
   if (threadIdx.x == 0) no_abort = 0;
   __syncthreads();
 
@@ -372,8 +380,8 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
             for (int i = 0; i < R; ++i) {
               const int row = r0 + i;
-              const bool vis = row < a.l_obs && key < a.l_prompt &&
-                               (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + row : key <= lim);
+              const bool vis = row < a.rows && key < a.l_prompt &&
+                               (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + (GQ ? row_pos[row] : row) : key <= lim);
               if (vis) v[i] = fmaxf(v[i], acc[i]);
             }
           }
@@ -405,8 +413,8 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
             for (int i = 0; i < R; ++i) {
               const int row = r0 + i;
-              const bool vis = row < a.l_obs && key < a.l_prompt &&
-                               (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + row : key <= lim);
+              const bool vis = row < a.rows && key < a.l_prompt &&
+                               (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + (GQ ? row_pos[row] : row) : key <= lim);
               if (vis) v[i] += ex2(fmaf(acc[i], a.scale_log2, -mrow[i]));
             }
           }
@@ -417,7 +425,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         stash_rows(v, r0);
         ptx::named_barrier(bar_id, 128);
         if (last_read && gtid == 0) ptx::mbar_arrive(&c.tmem_empty[slot]);
-        if (gtid < R && r0 + gtid < a.l_obs) {
+        if (gtid < R && r0 + gtid < a.rows) {
           float zz = gred[r0 + gtid];
 #pragma unroll
           for (int w = 1; w < 4; ++w) zz += gred[w * N + r0 + gtid];
@@ -430,7 +438,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
             const uint32_t fb = __float_as_uint(zz * ex2(mx - fl));
             const long long e = (long long)fminf(fmaxf(fl, -1000.f), 1000.f) + (long long)((fb >> 23) & 0xFF) - 127;
             const long long db = ((e + 1023) << 52) | ((long long)(fb & 0x7FFFFF) << 29);
-            ptx::red_add_f64(a.zsum + (int64_t)it.head * a.l_obs + r0 + gtid, __longlong_as_double(db));
+            ptx::red_add_f64(a.zsum + (int64_t)it.head * a.rows + r0 + gtid, __longlong_as_double(db));
           }
         }
         ptx::named_barrier(bar_id, 128);
@@ -462,9 +470,9 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       ptx::named_barrier(bar_id, 128);
       if (gtid < N) {
         float cv = INFINITY;   // rows past L_obs: zero logits, zero weight
-        if (gtid < a.l_obs) {
+        if (gtid < a.rows) {
           // log2 Z_i = exponent + log2(mantissa in [1, 2)), read off the fp64 bits
-          const long long zb = __double_as_longlong(__ldcg(a.zsum + (int64_t)it.head * a.l_obs + gtid));
+          const long long zb = __double_as_longlong(__ldcg(a.zsum + (int64_t)it.head * a.rows + gtid));
           const int e = (int)((zb >> 52) & 0x7FF) - 1023;
           const float mant = __uint_as_float(0x3F800000u | (uint32_t)((zb >> 29) & 0x7FFFFF));
           cv = (zb & 0x7FF0000000000000LL) ? (float)e + log2f(mant) : -INFINITY;
@@ -529,20 +537,22 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
   }
 }
 
-template <int D, int N>
+template <int D, int N, bool GQ>
 cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   using Lay = TcLayout<D, N>;
-  auto kern = vote_tc_kernel<D, N>;
+  auto kern = vote_tc_kernel<D, N, GQ>;
   if (grid <= 0) return cudaErrorInvalidConfiguration;   // tc_grid() also set the smem attribute
   cudaError_t err;
   CUtensorMap mk, mq;
   const int64_t bh = (int64_t)job.batch * job.heads;
-  if (!tc::make_map(&mk, job.k, D, job.l_prompt, bh, kTileKeys) || !tc::make_map(&mq, job.q_obs, D, job.l_obs, bh, N))
+  if (!tc::make_map(&mk, job.k, D, job.l_prompt, bh, kTileKeys) ||
+      !tc::make_map(&mq, job.q_obs, D, job.q_rows, bh, N))
     return cudaErrorInvalidValue;
   TcArgs a;
   a.l_prompt = job.l_prompt;
   a.l_prefix = job.l_prefix;
   a.l_obs = job.l_obs;
+  a.rows = job.q_rows;
   a.scope = job.scope;
   a.keys_per_item = Lay::TI * kTileKeys;
   a.n_chunk = (int)((job.l_prompt + a.keys_per_item - 1) / a.keys_per_item);
@@ -589,7 +599,7 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
 // columns), or 0 if the kernel cannot be resident. The answer depends only on the device and the
 // instantiation, so it is looked up once per (device, instantiation) and cached; the kernel's
 // shared-memory attribute is set at the same time.
-template <int D, int N>
+template <int D, int N, bool GQ>
 int tc_grid() {
   using Lay = TcLayout<D, N>;
   constexpr int kMaxDev = 64;
@@ -601,9 +611,9 @@ int tc_grid() {
   int sms = 0, per_sm = 0;
   int grid = -1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-      cudaFuncSetAttribute(vote_tc_kernel<D, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES) ==
+      cudaFuncSetAttribute(vote_tc_kernel<D, N, GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES) ==
           cudaSuccess &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vote_tc_kernel<D, N>, kThreadsTc, Lay::BYTES) ==
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vote_tc_kernel<D, N, GQ>, kThreadsTc, Lay::BYTES) ==
           cudaSuccess &&
       per_sm > 0)
     grid = sms;
@@ -612,36 +622,58 @@ int tc_grid() {
 }
 
 template <int D>
-int tc_n_pad(int l_obs) {
-  return l_obs <= 16 ? 16 : (l_obs <= 32 ? 32 : 64);
+int tc_n_pad(int rows) {
+  return rows <= 16 ? 16 : (rows <= 32 ? 32 : (rows <= 64 ? 64 : 128));
 }
 
 }  // namespace
 
-int vote_tc_keys_per_item(int l_obs) { return (128 / tc_n_pad<128>(l_obs)) * kTileKeys; }
+int vote_tc_keys_per_item(int q_rows, int l_obs) {
+  const int n = tc_n_pad<128>(q_rows);
+  return (128 / ((q_rows != l_obs && n < 64) ? 64 : n)) * kTileKeys;
+}
+
+// Instantiations: padded row count n of a single head's window (16, 32, 64, 128), or of a group of
+// query heads' windows (grouped: 64 or 128).
+template <int D>
+int tc_grid_n(int n, bool grouped) {
+  if (grouped) return n <= 64 ? tc_grid<D, 64, true>() : tc_grid<D, 128, true>();
+  return n == 16 ? tc_grid<D, 16, false>() : n == 32 ? tc_grid<D, 32, false>()
+                 : n == 64 ? tc_grid<D, 64, false>() : tc_grid<D, 128, false>();
+}
+
+template <int D>
+cudaError_t launch_tc_n(const CompressJob& job, int n, bool grouped) {
+  if (grouped)
+    return n <= 64 ? launch_tc_typed<D, 64, true>(job, tc_grid<D, 64, true>())
+                   : launch_tc_typed<D, 128, true>(job, tc_grid<D, 128, true>());
+  if (n == 16) return launch_tc_typed<D, 16, false>(job, tc_grid<D, 16, false>());
+  if (n == 32) return launch_tc_typed<D, 32, false>(job, tc_grid<D, 32, false>());
+  if (n == 64) return launch_tc_typed<D, 64, false>(job, tc_grid<D, 64, false>());
+  return launch_tc_typed<D, 128, false>(job, tc_grid<D, 128, false>());
+}
+
+// Padded row count the kernels use: grouped windows take 64 or 128 columns.
+static int tc_rows_pad(const CompressJob& job) {
+  return 128 * kTileKeys / vote_tc_keys_per_item(job.q_rows, job.l_obs);
+}
 
 bool vote_tc_eligible(const CompressJob& job) {
-  if (job.dtype != SNAPKV_BF16 || job.l_obs > 64) return false;
+  if (job.dtype != SNAPKV_BF16 || job.q_rows > 128) return false;
   if (job.head_dim != 64 && job.head_dim != 128) return false;
-  const int n = tc_n_pad<128>(job.l_obs);
-  const int grid = job.head_dim == 64 ? (n == 16 ? tc_grid<64, 16>() : n == 32 ? tc_grid<64, 32>() : tc_grid<64, 64>())
-                                      : (n == 16 ? tc_grid<128, 16>() : n == 32 ? tc_grid<128, 32>() : tc_grid<128, 64>());
+  const bool grouped = job.q_rows != job.l_obs;
+  const int n = tc_rows_pad(job);
+  const int grid = job.head_dim == 64 ? tc_grid_n<64>(n, grouped) : tc_grid_n<128>(n, grouped);
   if (grid <= 0) return false;
-  const int64_t per_item = vote_tc_keys_per_item(job.l_obs);
+  const int64_t per_item = (128 / n) * kTileKeys;
   const int64_t n_chunk = (job.l_prompt + per_item - 1) / per_item;
   return 2 * n_chunk * job.batch * job.heads < ((int64_t)1 << 31);
 }
 
 cudaError_t launch_vote_tc(const CompressJob& job) {
-  const int n = tc_n_pad<128>(job.l_obs);
-  if (job.head_dim == 64) {
-    if (n == 16) return launch_tc_typed<64, 16>(job, tc_grid<64, 16>());
-    if (n == 32) return launch_tc_typed<64, 32>(job, tc_grid<64, 32>());
-    return launch_tc_typed<64, 64>(job, tc_grid<64, 64>());
-  }
-  if (n == 16) return launch_tc_typed<128, 16>(job, tc_grid<128, 16>());
-  if (n == 32) return launch_tc_typed<128, 32>(job, tc_grid<128, 32>());
-  return launch_tc_typed<128, 64>(job, tc_grid<128, 64>());
+  const bool grouped = job.q_rows != job.l_obs;
+  const int n = tc_rows_pad(job);
+  return job.head_dim == 64 ? launch_tc_n<64>(job, n, grouped) : launch_tc_n<128>(job, n, grouped);
 }
 
 }  // namespace snapkv

@@ -76,6 +76,10 @@ def lib():
         L.snapkv_decode_attend.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, P, SZ, P, P]
         L.snapkv_decode_attend_noalloc.restype = I32
         L.snapkv_decode_attend_noalloc.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, P, P]
+        L.snapkv_compress_gqa_workspace_size.restype = SZ
+        L.snapkv_compress_gqa_workspace_size.argtypes = [PP, I32]
+        L.snapkv_compress_gqa.restype = I32
+        L.snapkv_compress_gqa.argtypes = [PP, I32, P, P, P, P, P, I64, P, P, P, P, SZ, P, P]
         L.snapkv_hit_rate.restype = I32
         L.snapkv_hit_rate.argtypes = [P, P, I64, P, I64, P, I64, I32, I32, I32, I32, ctypes.c_double, P, P, P, P]
         L.snapkv_status_string.restype = ctypes.c_char_p
@@ -126,8 +130,10 @@ def kept(params: CompressParams) -> int:
     return int(lib().snapkv_compress_kept(ctypes.byref(params)))
 
 
-def compress_workspace_size(params: CompressParams) -> int:
-    return int(lib().snapkv_compress_workspace_size(ctypes.byref(params)))
+def compress_workspace_size(params: CompressParams, q_heads=None) -> int:
+    if q_heads is None or q_heads == params.heads:
+        return int(lib().snapkv_compress_workspace_size(ctypes.byref(params)))
+    return int(lib().snapkv_compress_gqa_workspace_size(ctypes.byref(params), int(q_heads)))
 
 
 def decode_workspace_size(batch, heads, head_dim, cap) -> int:
@@ -143,14 +149,17 @@ def new_workspace(nbytes: int, device):
 def compress(q_obs, k, v, *, pool_kernel, ratio_p=0.0, budget=0, scope="prompt_causal", algo="auto", cap=None,
              k_out=None, v_out=None, len_out=None, idx_out=None, vote_out=None, want_idx=True,
              want_vote=False, workspace=None, dev_status=None, stream=None):
-    """snapkv_compress on torch tensors q_obs [B,H,L_obs,d], k, v [B,H,L_prompt,d].
+    """snapkv_compress on torch tensors q_obs [B,Hq,L_obs,d], k, v [B,H,L_prompt,d].
 
-    Returns a dict with k_out, v_out ([B,H,cap,d]), len_out [B], idx [B,H,k] (if wanted) and
-    vote [B,H,L_prefix] (if wanted), plus k (kept slots) and the workspace used.
+    Hq > H (a multiple of H) is grouped-query attention (snapkv_compress_gqa): the Hq / H query
+    heads of each KV head vote together. Returns a dict with k_out, v_out ([B,H,cap,d]), len_out
+    [B], idx [B,H,k] (if wanted) and vote [B,H,L_prefix] (if wanted), plus k (kept slots) and the
+    workspace used.
     """
     import torch
     B, H, L, d = k.shape
     l_obs = q_obs.shape[2]
+    q_heads = q_obs.shape[1]
     params = make_params(batch=B, heads=H, head_dim=d, l_obs=l_obs, l_prompt=L, pool_kernel=pool_kernel,
                          ratio_p=ratio_p, budget=budget, scope=scope, dtype=_dtype_code(k), algo=algo)
     ksel = kept(params)
@@ -169,18 +178,24 @@ def compress(q_obs, k, v, *, pool_kernel, ratio_p=0.0, budget=0, scope="prompt_c
         idx_out = torch.empty((B, H, max(ksel, 0)), dtype=torch.int32, device=dev)
     if vote_out is None and want_vote:
         vote_out = torch.empty((B, H, L - l_obs), dtype=torch.float32, device=dev)
-    need = compress_workspace_size(params)
+    need = compress_workspace_size(params, q_heads)
     if workspace is None:
         workspace = new_workspace(need, dev)
     for t in (q_obs, k, v, k_out, v_out):
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous")
-    st = lib().snapkv_compress(ctypes.byref(params), _ptr(q_obs), _ptr(k), _ptr(v), _ptr(k_out), _ptr(v_out),
-                               int(cap), _ptr(len_out), _ptr(idx_out) if ksel > 0 else None, _ptr(vote_out),
-                               _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
-                               _stream_handle(stream))
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if q_heads == H:
+        st = lib().snapkv_compress(ctypes.byref(params), _ptr(q_obs), _ptr(k), _ptr(v), _ptr(k_out), _ptr(v_out),
+                                   int(cap), _ptr(len_out), _ptr(idx_out) if ksel > 0 else None, _ptr(vote_out),
+                                   _ptr(workspace), ws_bytes, _ptr(dev_status), _stream_handle(stream))
+    else:
+        st = lib().snapkv_compress_gqa(ctypes.byref(params), int(q_heads), _ptr(q_obs), _ptr(k), _ptr(v),
+                                       _ptr(k_out), _ptr(v_out), int(cap), _ptr(len_out),
+                                       _ptr(idx_out) if ksel > 0 else None, _ptr(vote_out), _ptr(workspace),
+                                       ws_bytes, _ptr(dev_status), _stream_handle(stream))
     if st != OK:
-        raise SnapKVError(st, "snapkv_compress")
+        raise SnapKVError(st, "snapkv_compress" if q_heads == H else "snapkv_compress_gqa")
     return {"k_out": k_out, "v_out": v_out, "len": len_out, "idx": idx_out, "vote": vote_out, "k": ksel,
             "workspace": workspace, "cap": cap}
 

@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = sk.declared_functions()
-    assert len(names) == 11
+    assert len(names) == 13
     for n in names:
         assert hasattr(lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", sk.library_path()], capture_output=True, text=True).stdout
@@ -99,6 +99,19 @@ def test_decode_and_append_reject_bad_arguments(lib):
         == sk.ERR_WORKSPACE
     assert lib.snapkv_decode_attend(P(16), P(32), P(48), 10, P(64), P(88), 1, 1, 64, 0, P(256), 1 << 20, None,
                                     None) == sk.ERR_INVALID_ARG               # misaligned output
+
+
+def test_gqa_rejects_bad_groupings(lib):
+    P = ctypes.c_void_p
+    p = _params(heads=4)
+    ws = sk.compress_workspace_size(p, 8)
+    assert ws > sk.compress_workspace_size(p)               # more window rows per KV head
+    assert sk.compress_workspace_size(p, 6) == 0             # not a multiple of the KV heads
+    assert sk.compress_workspace_size(p, 20) == 0            # 5 x 32 window rows > 128
+    args = (P(16), P(32), P(48), P(64), P(80), 200, P(96), None, None, P(256), ws, None, None)
+    assert lib.snapkv_compress_gqa(ctypes.byref(p), 6, *args) == sk.ERR_INVALID_ARG
+    assert lib.snapkv_compress_gqa(ctypes.byref(p), 2, *args) == sk.ERR_INVALID_ARG   # fewer query heads
+    assert lib.snapkv_compress_gqa(ctypes.byref(p), 20, *args) == sk.ERR_UNSUPPORTED
 
 
 def test_hit_rate_rejects_bad_arguments(lib):

@@ -73,9 +73,12 @@ CompressLayout compress_layout(int batch, int heads, int l_obs, int q_rows, int6
   L.c = up256(bh * chunks * q_rows * 2 * sizeof(float));
   L.p = L.c + up256(bh * l_prefix * sizeof(float));
   L.idx = L.p + up256(bh * l_prefix * sizeof(float));
-  L.tc_zsum = L.idx + up256(bh * (k_sel > 0 ? k_sel : 1) * sizeof(int32_t));
+  const size_t group = (size_t)(q_rows / l_obs);   // query heads per KV head
+  // per-query-head votes of the tensor-core path under grouped-query attention
+  L.c_q = L.idx + up256(bh * (k_sel > 0 ? k_sel : 1) * sizeof(int32_t));
+  L.tc_zsum = L.c_q + (group > 1 ? up256(bh * group * l_prefix * sizeof(float)) : 0);
   L.tc_counters = L.tc_zsum + up256(bh * q_rows * sizeof(double));
-  L.total = L.tc_counters + up256(bh * sizeof(uint32_t));
+  L.total = L.tc_counters + up256(bh * group * sizeof(uint32_t));
   return L;
 }
 
@@ -185,6 +188,7 @@ snapkv_status compress_impl(const snapkv_compress_params* params, int32_t q_head
   job.c = vote_out ? vote_out : reinterpret_cast<float*>(ws + L.c);
   job.p = reinterpret_cast<float*>(ws + L.p);
   job.partial = reinterpret_cast<float*>(ws + L.partial);
+  job.c_q = reinterpret_cast<float*>(ws + L.c_q);
   job.tc_zsum = reinterpret_cast<double*>(ws + L.tc_zsum);
   job.tc_cnt = reinterpret_cast<uint32_t*>(ws + L.tc_counters);
   job.tc_zero_bytes = L.total - L.tc_zsum;

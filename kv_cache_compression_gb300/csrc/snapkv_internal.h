@@ -20,6 +20,7 @@ struct CompressJob {
   int32_t* len_out;
   int32_t* idx;        // kept indices (caller's buffer or workspace)
   float* c;            // vote (caller's buffer or workspace)
+  float* c_q;          // per-query-head votes under grouped-query attention (workspace)
   float* p;            // pooled vote (workspace)
   float* partial;      // per-chunk row statistics (workspace)
   double* tc_zsum;     // per-(head, row) fp64 sums of 2^(logit) (workspace; zeroed per call)
@@ -49,7 +50,7 @@ enum { kStageScore = 0, kStageVote = 1, kStageTopk = 2, kStageGather = 3, kStage
 
 // Workspace layout of a compression call (byte offsets, each 256-aligned).
 struct CompressLayout {
-  size_t partial, c, p, idx, tc_zsum, tc_counters, total;
+  size_t partial, c, p, idx, c_q, tc_zsum, tc_counters, total;
   int vote_chunk, n_chunk_all, n_chunk_prefix;
 };
 

@@ -1,6 +1,8 @@
-// Score + softmax + vote on the 5th-generation tensor cores (bf16, d = 64 or 128, at most 128
-// window-query rows per head: L_obs, or G * L_obs for G query heads sharing a KV head, whose rows
-// follow one another; row i sits at window position i mod L_obs and the vote sums every row).
+// Score + softmax + vote on the 5th-generation tensor cores (bf16, d = 64 or 128, L_obs <= 128).
+// Under grouped-query attention (G query heads per KV head) every query head is a head of its own
+// here, reading its KV head's keys (key tiles of the G heads of a group are fetched in the same
+// round of the queue, so the later ones hit in L2); its vote goes to a per-query-head buffer and a
+// second kernel adds the G votes of each KV head in a fixed order.
 //
 // SnapKV explainer ("論文解説: SnapKV"), sections 投票メカニズム and アルゴリズム: logits
 // s_ij = q_i . k_j / sqrt(d) of the L_obs window queries against every prompt key, the row
@@ -59,10 +61,11 @@ constexpr long long kDrainLimit = 400000000LL;
 
 struct TcArgs {
   int64_t l_prompt, l_prefix;
-  int l_obs, rows, scope, n_chunk, n_queue, keys_per_item, bh_total, delta;   // rows: window-query rows
+  int l_obs, scope, n_chunk, n_queue, keys_per_item, bh_total, delta;
+  int group;         // query heads per KV head: head h reads the keys of KV head h / group
   int resident;      // 1: one item per key chunk, logits stay in TMEM from statistics to vote
   float scale_log2;
-  double* zsum;      // [BH][rows]: Z_i = sum_j 2^(s'_ij) over the row's visible keys (fp64)
+  double* zsum;      // [BH][l_obs]: Z_i = sum_j 2^(s'_ij) over the head's visible keys (fp64)
   uint32_t* cnt;     // [BH] A items whose contribution to zsum is complete
   float* c_out;      // [BH][l_prefix]
   int32_t* dev_status;
@@ -161,10 +164,7 @@ __device__ __forceinline__ int tiles_of(const TcArgs& a, int chunk, int TI) {
   return t < TI ? t : TI;
 }
 
-// GQ: the rows are several query heads' windows (grouped-query attention), so a row's window
-// position is row mod L_obs (looked up in a table); otherwise it is the row itself. The two are
-// separate instantiations: the table lookup in the window tiles slows the common case's epilogue.
-template <int D, int N, bool GQ>
+template <int D, int N>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q, TcArgs a) {
   using Lay = TcLayout<D, N>;
@@ -200,9 +200,6 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
   ptx::tc_fence_after();
   const uint32_t tmem_base = c.misc[0];
   __shared__ int no_abort;
-  __shared__ int row_pos[GQ ? N : 1];   // window position of each query row (row mod L_obs)
-  if (GQ)
-    for (int i = threadIdx.x; i < N; i += kThreadsTc) row_pos[i] = i % a.l_obs;
   if (threadIdx.x == 0) no_abort = 0;
   __syncthreads();
 
@@ -245,7 +242,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
           for (int kb = 0; kb < Lay::KB; ++kb)
             ptx::tma_load_3d_hint(base + Lay::OFF_K + stage * Lay::STAGE_BYTES + kb * Lay::A_BYTES, &tmap_k,
-                                  kb * 64, key0 + t * kTileKeys, it.head, &c.full[stage], policy);
+                                  kb * 64, key0 + t * kTileKeys, it.head / a.group, &c.full[stage], policy);
         }
         if (!ok) {
           ++n;
@@ -380,8 +377,8 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
             for (int i = 0; i < R; ++i) {
               const int row = r0 + i;
-              const bool vis = row < a.rows && key < a.l_prompt &&
-                               (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + (GQ ? row_pos[row] : row) : key <= lim);
+              const bool vis = row < a.l_obs && key < a.l_prompt &&
+                               (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + row : key <= lim);
               if (vis) v[i] = fmaxf(v[i], acc[i]);
             }
           }
@@ -413,8 +410,8 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
             for (int i = 0; i < R; ++i) {
               const int row = r0 + i;
-              const bool vis = row < a.rows && key < a.l_prompt &&
-                               (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + (GQ ? row_pos[row] : row) : key <= lim);
+              const bool vis = row < a.l_obs && key < a.l_prompt &&
+                               (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + row : key <= lim);
               if (vis) v[i] += ex2(fmaf(acc[i], a.scale_log2, -mrow[i]));
             }
           }
@@ -425,7 +422,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         stash_rows(v, r0);
         ptx::named_barrier(bar_id, 128);
         if (last_read && gtid == 0) ptx::mbar_arrive(&c.tmem_empty[slot]);
-        if (gtid < R && r0 + gtid < a.rows) {
+        if (gtid < R && r0 + gtid < a.l_obs) {
           float zz = gred[r0 + gtid];
 #pragma unroll
           for (int w = 1; w < 4; ++w) zz += gred[w * N + r0 + gtid];
@@ -438,7 +435,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
             const uint32_t fb = __float_as_uint(zz * ex2(mx - fl));
             const long long e = (long long)fminf(fmaxf(fl, -1000.f), 1000.f) + (long long)((fb >> 23) & 0xFF) - 127;
             const long long db = ((e + 1023) << 52) | ((long long)(fb & 0x7FFFFF) << 29);
-            ptx::red_add_f64(a.zsum + (int64_t)it.head * a.rows + r0 + gtid, __longlong_as_double(db));
+            ptx::red_add_f64(a.zsum + (int64_t)it.head * a.l_obs + r0 + gtid, __longlong_as_double(db));
           }
         }
         ptx::named_barrier(bar_id, 128);
@@ -470,9 +467,9 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       ptx::named_barrier(bar_id, 128);
       if (gtid < N) {
         float cv = INFINITY;   // rows past L_obs: zero logits, zero weight
-        if (gtid < a.rows) {
+        if (gtid < a.l_obs) {
           // log2 Z_i = exponent + log2(mantissa in [1, 2)), read off the fp64 bits
-          const long long zb = __double_as_longlong(__ldcg(a.zsum + (int64_t)it.head * a.rows + gtid));
+          const long long zb = __double_as_longlong(__ldcg(a.zsum + (int64_t)it.head * a.l_obs + gtid));
           const int e = (int)((zb >> 52) & 0x7FF) - 1023;
           const float mant = __uint_as_float(0x3F800000u | (uint32_t)((zb >> 29) & 0x7FFFFF));
           cv = (zb & 0x7FF0000000000000LL) ? (float)e + log2f(mant) : -INFINITY;
@@ -537,22 +534,37 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
   }
 }
 
-template <int D, int N, bool GQ>
+// Vote of each KV head = the sum of its G query heads' votes, added in query-head order.
+__global__ void __launch_bounds__(256)
+group_sum_kernel(const float* __restrict__ c_q, float* __restrict__ c, int64_t l_prefix, int64_t bh_kv, int group) {
+  const int64_t total = bh_kv * l_prefix;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t h = u / l_prefix, j = u - h * l_prefix;
+    const float* src = c_q + h * group * l_prefix + j;
+    float sum = 0.f;
+    for (int g = 0; g < group; ++g) sum += __ldcg(src + g * l_prefix);
+    c[u] = sum;
+  }
+}
+
+template <int D, int N>
 cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   using Lay = TcLayout<D, N>;
-  auto kern = vote_tc_kernel<D, N, GQ>;
+  auto kern = vote_tc_kernel<D, N>;
   if (grid <= 0) return cudaErrorInvalidConfiguration;   // tc_grid() also set the smem attribute
   cudaError_t err;
   CUtensorMap mk, mq;
-  const int64_t bh = (int64_t)job.batch * job.heads;
-  if (!tc::make_map(&mk, job.k, D, job.l_prompt, bh, kTileKeys) ||
-      !tc::make_map(&mq, job.q_obs, D, job.q_rows, bh, N))
+  const int group = job.q_rows / job.l_obs;                 // query heads per KV head
+  const int64_t bh_kv = (int64_t)job.batch * job.heads;
+  const int64_t bh = bh_kv * group;                           // query heads: the kernel's heads
+  if (!tc::make_map(&mk, job.k, D, job.l_prompt, bh_kv, kTileKeys) ||
+      !tc::make_map(&mq, job.q_obs, D, job.l_obs, bh, N))
     return cudaErrorInvalidValue;
   TcArgs a;
   a.l_prompt = job.l_prompt;
   a.l_prefix = job.l_prefix;
   a.l_obs = job.l_obs;
-  a.rows = job.q_rows;
+  a.group = group;
   a.scope = job.scope;
   a.keys_per_item = Lay::TI * kTileKeys;
   a.n_chunk = (int)((job.l_prompt + a.keys_per_item - 1) / a.keys_per_item);
@@ -570,7 +582,7 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)job.head_dim));
   a.zsum = job.tc_zsum;
   a.cnt = job.tc_cnt;
-  a.c_out = job.c;
+  a.c_out = group > 1 ? job.c_q : job.c;
   a.dev_status = job.dev_status;
   if (grid > a.n_queue) grid = a.n_queue;
   cudaLaunchConfig_t cfg = {};
@@ -591,6 +603,13 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   err = cudaLaunchKernelEx(&cfg, kern, mk, mq, a);
   job.mark(2 * kStageScore + 1);
   job.mark(2 * kStageVote);
+  if (err == cudaSuccess && group > 1) {
+    const int64_t total = bh_kv * job.l_prefix;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    group_sum_kernel<<<(unsigned)blocks, 256, 0, job.stream>>>(job.c_q, job.c, job.l_prefix, bh_kv, group);
+    err = cudaGetLastError();
+  }
   job.mark(2 * kStageVote + 1);
   return err;
 }
@@ -599,7 +618,7 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
 // columns), or 0 if the kernel cannot be resident. The answer depends only on the device and the
 // instantiation, so it is looked up once per (device, instantiation) and cached; the kernel's
 // shared-memory attribute is set at the same time.
-template <int D, int N, bool GQ>
+template <int D, int N>
 int tc_grid() {
   using Lay = TcLayout<D, N>;
   constexpr int kMaxDev = 64;
@@ -611,9 +630,9 @@ int tc_grid() {
   int sms = 0, per_sm = 0;
   int grid = -1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-      cudaFuncSetAttribute(vote_tc_kernel<D, N, GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES) ==
+      cudaFuncSetAttribute(vote_tc_kernel<D, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES) ==
           cudaSuccess &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vote_tc_kernel<D, N, GQ>, kThreadsTc, Lay::BYTES) ==
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vote_tc_kernel<D, N>, kThreadsTc, Lay::BYTES) ==
           cudaSuccess &&
       per_sm > 0)
     grid = sms;
@@ -629,51 +648,38 @@ int tc_n_pad(int rows) {
 }  // namespace
 
 int vote_tc_keys_per_item(int q_rows, int l_obs) {
-  const int n = tc_n_pad<128>(q_rows);
-  return (128 / ((q_rows != l_obs && n < 64) ? 64 : n)) * kTileKeys;
-}
-
-// Instantiations: padded row count n of a single head's window (16, 32, 64, 128), or of a group of
-// query heads' windows (grouped: 64 or 128).
-template <int D>
-int tc_grid_n(int n, bool grouped) {
-  if (grouped) return n <= 64 ? tc_grid<D, 64, true>() : tc_grid<D, 128, true>();
-  return n == 16 ? tc_grid<D, 16, false>() : n == 32 ? tc_grid<D, 32, false>()
-                 : n == 64 ? tc_grid<D, 64, false>() : tc_grid<D, 128, false>();
+  (void)q_rows;   // grouped query heads are separate heads of l_obs rows here
+  return (128 / tc_n_pad<128>(l_obs)) * kTileKeys;
 }
 
 template <int D>
-cudaError_t launch_tc_n(const CompressJob& job, int n, bool grouped) {
-  if (grouped)
-    return n <= 64 ? launch_tc_typed<D, 64, true>(job, tc_grid<D, 64, true>())
-                   : launch_tc_typed<D, 128, true>(job, tc_grid<D, 128, true>());
-  if (n == 16) return launch_tc_typed<D, 16, false>(job, tc_grid<D, 16, false>());
-  if (n == 32) return launch_tc_typed<D, 32, false>(job, tc_grid<D, 32, false>());
-  if (n == 64) return launch_tc_typed<D, 64, false>(job, tc_grid<D, 64, false>());
-  return launch_tc_typed<D, 128, false>(job, tc_grid<D, 128, false>());
+int tc_grid_n(int n) {
+  return n == 16 ? tc_grid<D, 16>() : n == 32 ? tc_grid<D, 32>() : n == 64 ? tc_grid<D, 64>() : tc_grid<D, 128>();
 }
 
-// Padded row count the kernels use: grouped windows take 64 or 128 columns.
-static int tc_rows_pad(const CompressJob& job) {
-  return 128 * kTileKeys / vote_tc_keys_per_item(job.q_rows, job.l_obs);
+template <int D>
+cudaError_t launch_tc_n(const CompressJob& job, int n) {
+  if (n == 16) return launch_tc_typed<D, 16>(job, tc_grid<D, 16>());
+  if (n == 32) return launch_tc_typed<D, 32>(job, tc_grid<D, 32>());
+  if (n == 64) return launch_tc_typed<D, 64>(job, tc_grid<D, 64>());
+  return launch_tc_typed<D, 128>(job, tc_grid<D, 128>());
 }
 
 bool vote_tc_eligible(const CompressJob& job) {
-  if (job.dtype != SNAPKV_BF16 || job.q_rows > 128) return false;
+  if (job.dtype != SNAPKV_BF16 || job.l_obs > 128) return false;
   if (job.head_dim != 64 && job.head_dim != 128) return false;
-  const bool grouped = job.q_rows != job.l_obs;
-  const int n = tc_rows_pad(job);
-  const int grid = job.head_dim == 64 ? tc_grid_n<64>(n, grouped) : tc_grid_n<128>(n, grouped);
+  const int n = tc_n_pad<128>(job.l_obs);
+  const int grid = job.head_dim == 64 ? tc_grid_n<64>(n) : tc_grid_n<128>(n);
   if (grid <= 0) return false;
-  const int64_t per_item = (128 / n) * kTileKeys;
+  const int64_t per_item = vote_tc_keys_per_item(job.q_rows, job.l_obs);
   const int64_t n_chunk = (job.l_prompt + per_item - 1) / per_item;
-  return 2 * n_chunk * job.batch * job.heads < ((int64_t)1 << 31);
+  const int64_t q_heads = (int64_t)job.batch * job.heads * (job.q_rows / job.l_obs);
+  return 2 * n_chunk * q_heads < ((int64_t)1 << 31);
 }
 
 cudaError_t launch_vote_tc(const CompressJob& job) {
-  const bool grouped = job.q_rows != job.l_obs;
-  const int n = tc_rows_pad(job);
-  return job.head_dim == 64 ? launch_tc_n<64>(job, n, grouped) : launch_tc_n<128>(job, n, grouped);
+  const int n = tc_n_pad<128>(job.l_obs);
+  return job.head_dim == 64 ? launch_tc_n<64>(job, n) : launch_tc_n<128>(job, n);
 }
 
 }  // namespace snapkv

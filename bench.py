@@ -589,7 +589,7 @@ def run_ours(args, rank, world, local_rank):
     sv_ms = stage_mean["score"] + (0.0 if vote_fused else stage_mean["vote"])
     dom_ms = sv_ms if dominant == "score+vote" else stage_mean[dominant]
     dom_bytes = alg[dominant] * heads if alg.get(dominant) else 0
-    traffic, src_hash = profiled_traffic(["vote_tc.cu", "sm100_ptx.cuh", "snapkv_common.cuh"])
+    traffic, src_hash = profiled_traffic(["vote_tc.cu", "tc_common.cuh", "sm100_ptx.cuh", "snapkv_common.cuh"])
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_bytes else None
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": (achieved / peak) if achieved else None, "peak_source": f"{peak_kind} hbm_gbs",

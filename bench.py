@@ -661,7 +661,7 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "path": "pinned host Q/K/V -> device, snapkv.compress + append + decode_attend, "
                         "K_c/V_c/idx/out -> pinned host"},
-        "gpu_launches": args.steps * 5,
+        "gpu_launches": args.steps * 4,   # vote, top-k (+ gather), append, decode
         "clocks": clocks,
         "wall_s_timed": wall,
         "kernel_source_sha256_16": src_hash,

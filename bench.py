@@ -400,6 +400,47 @@ def gqa_compress(torch, snapkv, synth, dev, copies=4):
             "l2": f"{copies} input copies rotated ({copies * 2 * k_bytes / 2**20:.0f} MiB of K/V > L2)"}
 
 
+def varlen_compress(torch, snapkv, synth, dev, nseq=16, ratio_p=0.125):
+    """One snapkv_compress_varlen call over the first 16 prompts of the ragged-prompt decode workload
+    (L_prompt drawn from U{4096..32768}, H32 d128 bf16, L_obs 32, K_pool 7) under the ratio rule
+    p = 0.125, so that every sequence keeps its own number of rows. Inputs are padded to the longest
+    prompt (several GB of K/V, far above L2); the call is captured as a CUDA graph and events time 10
+    replays."""
+    wl = synth.WORKLOADS[4]
+    lengths = wl.prompt_lengths()[:nseq]
+    q, k, v = synth.device_inputs_padded(wl, 0, 0, lengths, dev, pad_value=0.0)
+    res = snapkv.compress_varlen(q, k, v, lengths, pool_kernel=wl.pool_kernel, ratio_p=ratio_p)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.synchronize(dev)
+
+    def call():
+        snapkv.compress_varlen(q, k, v, lengths, pool_kernel=wl.pool_kernel, ratio_p=ratio_p, out=res, stream=stream)
+    with torch.cuda.stream(stream):
+        call()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / 10
+    H, d, lo, eb = wl.heads, wl.head_dim, wl.l_obs, 2
+    alg = sum(H * (eb * d * (L + lo) + 2 * 2 * (kb + lo) * d * eb + 4 * kb) for L, kb in zip(lengths, res["ks"]))
+    tok_heads = sum(lengths) * H
+    del q, k, v, res, g
+    torch.cuda.empty_cache()
+    return {"workload": f"ragged prompts: {nseq} sequences, L_prompt U{{4096..32768}} (total {sum(lengths)}), "
+                        f"H32 d128 bf16, L_obs 32, K_pool 7, p {ratio_p} (k per sequence)",
+            "ms_per_call": ms, "tok_head_per_s": tok_heads / (ms * 1e-3), "alg_bytes": alg,
+            "alg_gbs": alg / (ms * 1e-3) / 1e9}
+
+
 def timing_event(torch):
     """A timing event that, recorded inside a stream capture, becomes an event-record node."""
     try:
@@ -633,6 +674,7 @@ def run_ours(args, rank, world, local_rank):
     full_cache = full_cache_decode(torch, snapkv, synth, dev) if world == 1 else None
     hit = hit_rate_diagnostic(torch, snapkv, synth, dev, *copies[0], wl) if world == 1 else None
     gqa = gqa_compress(torch, snapkv, synth, dev) if world == 1 else None
+    varlen = varlen_compress(torch, snapkv, synth, dev) if world == 1 else None
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
@@ -650,6 +692,7 @@ def run_ours(args, rank, world, local_rank):
         "full_cache_decode": full_cache,
         "hit_rate": hit,
         "gqa": gqa,
+        "varlen": varlen,
         "hbm_gbs_algorithmic_step": alg["step"] * heads / (ms_per_step * 1e-3) / 1e9,
         "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
         "stage_ms_note": stage_method + ("; the vote runs inside the score kernel" if vote_fused else "") +

@@ -178,6 +178,33 @@ SNAPKV_API snapkv_status snapkv_compress_gqa(const snapkv_compress_params* param
                                              int32_t* dev_status, snapkv_stream_t stream);
 
 /*
+ * snapkv_compress_varlen — snapkv_compress of a batch whose prompts have different lengths: sequence
+ * b has l_prompts[b] rows (host array, L_obs < l_prompts[b] <= params->l_prompt), so its prefix,
+ * its window (the last L_obs of its own rows) and its k = floor(p * L_prefix_b) or
+ * min(budget, L_prefix_b) ([SnapKV] 投票メカニズム) are its own. Each sequence is compressed as in
+ * snapkv_compress, one after another on `stream`, into its slice of the shared outputs.
+ *
+ * q_obs     device [B, H, L_obs, d]   each sequence's window queries
+ * k, v      device [B, H, params->l_prompt, d], padded: sequence b's rows 0 .. l_prompts[b]-1 are read
+ * k_out, v_out device [B, H, cap, d], cap >= k_max + L_obs where k_max = snapkv_compress_kept(params)
+ *           (k grows with the prompt length); rows 0 .. k_b + L_obs - 1 of sequence b are written
+ * len_out   device int32 [B], set to k_b + L_obs
+ * idx_out   device int32 [B, H, k_max] (NULL: not returned); sequence b's heads hold k_b indices
+ *           (ascending), the rest of each row is left untouched
+ * vote_out  device fp32 [B, H, L_prefix_max] (NULL: not returned), L_prefix_max = params->l_prompt -
+ *           L_obs; sequence b's heads hold L_prefix_b values, the rest is left untouched
+ * workspace >= snapkv_compress_varlen_workspace_size(params, l_prompts) bytes, 256-byte aligned
+ * A length outside (L_obs, params->l_prompt] gives SNAPKV_ERR_INVALID_ARG (and a workspace size of 0).
+ */
+SNAPKV_API size_t snapkv_compress_varlen_workspace_size(const snapkv_compress_params* params,
+                                                        const int64_t* l_prompts);
+SNAPKV_API snapkv_status snapkv_compress_varlen(const snapkv_compress_params* params, const int64_t* l_prompts,
+                                                const void* q_obs, const void* k, const void* v, void* k_out,
+                                                void* v_out, int64_t cap, int32_t* len_out, int32_t* idx_out,
+                                                float* vote_out, void* workspace, size_t workspace_bytes,
+                                                int32_t* dev_status, snapkv_stream_t stream);
+
+/*
  * snapkv_append — one decode step's cache append ([KVcache] 22.2): for every sequence b and
  * head h, row len[b] of k_cache / v_cache receives k_new / v_new, then len[b] += 1.
  *

@@ -135,6 +135,34 @@ size_t snapkv_compress_workspace_size(const snapkv_compress_params* params) {
 
 namespace {
 
+// The stage kernels of one validated compression job, in stream order.
+snapkv_status run_compress(const CompressJob& job, int algo) {
+  const bool cl_ok = algo == SNAPKV_ALGO_TENSOR_CORE_CLUSTER && vote_cluster_eligible(job);
+  const bool tc_ok = (algo == SNAPKV_ALGO_AUTO || algo == SNAPKV_ALGO_TENSOR_CORE) && vote_tc_eligible(job);
+  const bool tc_only = algo == SNAPKV_ALGO_TENSOR_CORE || algo == SNAPKV_ALGO_TENSOR_CORE_CLUSTER;
+  if (tc_only && !cl_ok && !tc_ok) return SNAPKV_ERR_UNSUPPORTED;
+  bool voted = false;
+  if (cl_ok) {
+    if (launch_vote_cluster(job) == cudaSuccess) voted = true;
+    else cudaGetLastError();   // a refused launch is not sticky; try the next kernel
+  }
+  if (!voted && tc_ok) {
+    if (launch_vote_tc(job) == cudaSuccess) voted = true;
+    else cudaGetLastError();
+  }
+  if (!voted && tc_only) return SNAPKV_ERR_CUDA;
+  if (!voted && launch_vote_simt(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  bool gathered = false;
+  if (launch_pool_topk(job, &gathered) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  if (gathered) {   // the gather stage ran inside the top-k kernel
+    job.mark(2 * kStageGather);
+    job.mark(2 * kStageGather + 1);
+  } else if (launch_gather(job) != cudaSuccess) {
+    return SNAPKV_ERR_CUDA;
+  }
+  return SNAPKV_OK;
+}
+
 snapkv_status compress_impl(const snapkv_compress_params* params, int32_t q_heads, const void* q_obs, const void* k,
                             const void* v, void* k_out, void* v_out, int64_t cap, int32_t* len_out, int32_t* idx_out,
                             float* vote_out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
@@ -175,6 +203,7 @@ snapkv_status compress_impl(const snapkv_compress_params* params, int32_t q_head
   job.scope = params->softmax_scope;
   job.dtype = params->dtype;
   job.l_prompt = params->l_prompt;
+  job.kv_stride = params->l_prompt;
   job.l_prefix = l_prefix;
   job.k_sel = k_sel;
   job.cap = cap;
@@ -200,31 +229,7 @@ snapkv_status compress_impl(const snapkv_compress_params* params, int32_t q_head
   job.events = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(stage_events));
   job.n_events = n_events;
 
-  const int algo = params->algo;
-  const bool cl_ok = algo == SNAPKV_ALGO_TENSOR_CORE_CLUSTER && vote_cluster_eligible(job);
-  const bool tc_ok = (algo == SNAPKV_ALGO_AUTO || algo == SNAPKV_ALGO_TENSOR_CORE) && vote_tc_eligible(job);
-  const bool tc_only = algo == SNAPKV_ALGO_TENSOR_CORE || algo == SNAPKV_ALGO_TENSOR_CORE_CLUSTER;
-  if (tc_only && !cl_ok && !tc_ok) return SNAPKV_ERR_UNSUPPORTED;
-  bool voted = false;
-  if (cl_ok) {
-    if (launch_vote_cluster(job) == cudaSuccess) voted = true;
-    else cudaGetLastError();   // a refused launch is not sticky; try the next kernel
-  }
-  if (!voted && tc_ok) {
-    if (launch_vote_tc(job) == cudaSuccess) voted = true;
-    else cudaGetLastError();
-  }
-  if (!voted && tc_only) return SNAPKV_ERR_CUDA;
-  if (!voted && launch_vote_simt(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
-  bool gathered = false;
-  if (launch_pool_topk(job, &gathered) != cudaSuccess) return SNAPKV_ERR_CUDA;
-  if (gathered) {   // the gather stage ran inside the top-k kernel
-    job.mark(2 * kStageGather);
-    job.mark(2 * kStageGather + 1);
-  } else if (launch_gather(job) != cudaSuccess) {
-    return SNAPKV_ERR_CUDA;
-  }
-  return SNAPKV_OK;
+  return run_compress(job, params->algo);
 }
 
 }  // namespace
@@ -247,6 +252,111 @@ snapkv_status snapkv_compress_gqa(const snapkv_compress_params* params, int32_t 
                                   size_t workspace_bytes, int32_t* dev_status, snapkv_stream_t stream) {
   return compress_impl(params, q_heads, q_obs, k, v, k_out, v_out, cap, len_out, idx_out, vote_out, workspace,
                        workspace_bytes, dev_status, stream, nullptr, 0);
+}
+
+size_t snapkv_compress_varlen_workspace_size(const snapkv_compress_params* params, const int64_t* l_prompts) {
+  int64_t lp = 0, k = 0;
+  int rows = 0;
+  if (!params || !l_prompts || check_params(params, params->heads, &lp, &k, &rows) != SNAPKV_OK) return 0;
+  size_t need = 0;
+  for (int32_t b = 0; b < params->batch; ++b) {
+    snapkv_compress_params pb = *params;
+    pb.batch = 1;
+    pb.l_prompt = l_prompts[b];
+    if (pb.l_prompt > params->l_prompt || check_params(&pb, pb.heads, &lp, &k, &rows) != SNAPKV_OK) return 0;
+    const size_t t = compress_layout(1, pb.heads, pb.l_obs, rows, pb.l_prompt, k).total;
+    if (t > need) need = t;
+  }
+  return need;
+}
+
+snapkv_status snapkv_compress_varlen(const snapkv_compress_params* params, const int64_t* l_prompts,
+                                     const void* q_obs, const void* k, const void* v, void* k_out, void* v_out,
+                                     int64_t cap, int32_t* len_out, int32_t* idx_out, float* vote_out,
+                                     void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                     snapkv_stream_t stream) {
+  int64_t lp_max = 0, k_max = 0;
+  int rows = 0;
+  if (!params || !l_prompts) return SNAPKV_ERR_INVALID_ARG;
+  const snapkv_status st = check_params(params, params->heads, &lp_max, &k_max, &rows);
+  if (st != SNAPKV_OK) return st;
+  if (!q_obs || !k || !v || !k_out || !v_out || !len_out) return SNAPKV_ERR_INVALID_ARG;
+  if (!aligned16(q_obs) || !aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out))
+    return SNAPKV_ERR_INVALID_ARG;
+  if (((uintptr_t)len_out & 3u) || ((uintptr_t)idx_out & 3u) || ((uintptr_t)vote_out & 3u) ||
+      ((uintptr_t)dev_status & 3u))
+    return SNAPKV_ERR_INVALID_ARG;
+  const size_t need = snapkv_compress_varlen_workspace_size(params, l_prompts);
+  if (need == 0) return SNAPKV_ERR_INVALID_ARG;   // a sequence length outside [L_obs + 1, params->l_prompt]
+  if (cap < k_max + params->l_obs || cap > kMaxPrompt) return SNAPKV_ERR_CAPACITY;   // k grows with L
+  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u)) return SNAPKV_ERR_WORKSPACE;
+  const size_t esize = params->dtype == SNAPKV_BF16 ? 2 : 4;
+  const size_t H = (size_t)params->heads, d = (size_t)params->head_dim;
+  const size_t in_bytes = params->batch * H * (size_t)params->l_prompt * d * esize;
+  const size_t out_bytes = params->batch * H * (size_t)cap * d * esize;
+  if (overlaps(k, in_bytes, k_out, out_bytes) || overlaps(k, in_bytes, v_out, out_bytes) ||
+      overlaps(v, in_bytes, k_out, out_bytes) || overlaps(v, in_bytes, v_out, out_bytes) ||
+      overlaps(k_out, out_bytes, v_out, out_bytes))
+    return SNAPKV_ERR_INVALID_ARG;
+
+  const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  for (int32_t b = 0; b < params->batch; ++b) {
+    snapkv_compress_params pb = *params;
+    pb.batch = 1;
+    pb.l_prompt = l_prompts[b];
+    int64_t l_prefix = 0, k_sel = 0;
+    int q_rows = 0;
+    check_params(&pb, pb.heads, &l_prefix, &k_sel, &q_rows);   // validated above
+    const CompressLayout L = compress_layout(1, pb.heads, pb.l_obs, q_rows, pb.l_prompt, k_sel);
+    CompressJob job;
+    job.batch = 1;
+    job.heads = pb.heads;
+    job.head_dim = pb.head_dim;
+    job.l_obs = pb.l_obs;
+    job.q_rows = q_rows;
+    job.pool_kernel = pb.pool_kernel;
+    job.scope = pb.softmax_scope;
+    job.dtype = pb.dtype;
+    job.l_prompt = pb.l_prompt;
+    job.kv_stride = params->l_prompt;   // the padded batch's row stride
+    job.l_prefix = l_prefix;
+    job.k_sel = k_sel;
+    job.cap = cap;
+    job.q_obs = static_cast<const char*>(q_obs) + (size_t)b * H * pb.l_obs * d * esize;
+    job.k = static_cast<const char*>(k) + (size_t)b * H * params->l_prompt * d * esize;
+    job.v = static_cast<const char*>(v) + (size_t)b * H * params->l_prompt * d * esize;
+    job.k_out = static_cast<char*>(k_out) + (size_t)b * H * cap * d * esize;
+    job.v_out = static_cast<char*>(v_out) + (size_t)b * H * cap * d * esize;
+    job.len_out = len_out + b;
+    job.idx = reinterpret_cast<int32_t*>(ws + L.idx);
+    job.c = reinterpret_cast<float*>(ws + L.c);
+    job.p = reinterpret_cast<float*>(ws + L.p);
+    job.partial = reinterpret_cast<float*>(ws + L.partial);
+    job.c_q = reinterpret_cast<float*>(ws + L.c_q);
+    job.tc_zsum = reinterpret_cast<double*>(ws + L.tc_zsum);
+    job.tc_cnt = reinterpret_cast<uint32_t*>(ws + L.tc_counters);
+    job.tc_zero_bytes = L.total - L.tc_zsum;
+    job.vote_chunk = L.vote_chunk;
+    job.n_chunk_all = L.n_chunk_all;
+    job.n_chunk_prefix = L.n_chunk_prefix;
+    job.dev_status = dev_status;
+    job.stream = strm;
+    job.events = nullptr;
+    job.n_events = 0;
+    const snapkv_status r = run_compress(job, pb.algo);
+    if (r != SNAPKV_OK) return r;
+    // This sequence's indices and vote into the caller's [B, H, k_max] and [B, H, L_prefix_max].
+    if (idx_out && k_sel > 0 &&
+        cudaMemcpy2DAsync(idx_out + (size_t)b * H * k_max, (size_t)k_max * 4, job.idx, (size_t)k_sel * 4,
+                          (size_t)k_sel * 4, H, cudaMemcpyDeviceToDevice, strm) != cudaSuccess)
+      return SNAPKV_ERR_CUDA;
+    if (vote_out &&
+        cudaMemcpy2DAsync(vote_out + (size_t)b * H * lp_max, (size_t)lp_max * 4, job.c, (size_t)l_prefix * 4,
+                          (size_t)l_prefix * 4, H, cudaMemcpyDeviceToDevice, strm) != cudaSuccess)
+      return SNAPKV_ERR_CUDA;
+  }
+  return SNAPKV_OK;
 }
 
 snapkv_status snapkv_compress(const snapkv_compress_params* params, const void* q_obs, const void* k,

@@ -13,7 +13,8 @@ namespace {
 __global__ void __launch_bounds__(256)
 gather_window_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* __restrict__ k_out,
                      uint4* __restrict__ v_out, const int32_t* __restrict__ idx, int32_t* __restrict__ len_out,
-                     int batch, int heads, int64_t l_prompt, int64_t l_prefix, int64_t k_sel, int64_t rows_out,
+                     int batch, int heads, int64_t kv_stride, int64_t l_prompt, int64_t l_prefix, int64_t k_sel,
+                     int64_t rows_out,
                      int64_t cap, int vpr, int32_t* __restrict__ dev_status) {
   const int64_t per_head = rows_out * vpr;
   const int64_t total = (int64_t)batch * heads * per_head;
@@ -30,7 +31,7 @@ gather_window_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, u
       report(dev_status, SNAPKV_ERR_INTERNAL);
       continue;
     }
-    const int64_t in_at = (bh * l_prompt + src) * vpr + c;
+    const int64_t in_at = (bh * kv_stride + src) * vpr + c;
     const int64_t out_at = (bh * cap + r) * vpr + c;
     const uint4 kv = ld_stream_v4(k + in_at);
     const uint4 vv = ld_stream_v4(v + in_at);
@@ -56,7 +57,8 @@ cudaError_t launch_gather(const CompressJob& job) {
   job.mark(2 * kStageGather);
   gather_window_kernel<<<(unsigned)blocks, 256, 0, job.stream>>>(
       static_cast<const uint4*>(job.k), static_cast<const uint4*>(job.v), static_cast<uint4*>(job.k_out),
-      static_cast<uint4*>(job.v_out), job.idx, job.len_out, job.batch, job.heads, job.l_prompt, job.l_prefix,
+      static_cast<uint4*>(job.v_out), job.idx, job.len_out, job.batch, job.heads, job.kv_stride, job.l_prompt,
+      job.l_prefix,
       job.k_sel, rows_out, job.cap, vpr, job.dev_status);
   job.mark(2 * kStageGather + 1);
   return cudaGetLastError();

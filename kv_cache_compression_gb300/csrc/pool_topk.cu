@@ -222,7 +222,7 @@ struct GatherArgs {
   uint4* k_out;
   uint4* v_out;
   int32_t* len_out;
-  int64_t l_prompt, cap;
+  int64_t kv_stride, cap;   // rows between heads in k / v, rows per head in k_out / v_out
   int vpr, l_obs, heads;
 };
 
@@ -374,8 +374,8 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   // Gather: this CTA's kept rows, then window rows rank, rank + csize, ... (16-byte pieces, four
   // rows' worth of loads in flight per thread).
   const int vpr = g.vpr;
-  const uint4* kin = g.k + bh * g.l_prompt * vpr;
-  const uint4* vin = g.v + bh * g.l_prompt * vpr;
+  const uint4* kin = g.k + bh * g.kv_stride * vpr;
+  const uint4* vin = g.v + bh * g.kv_stride * vpr;
   uint4* kout = g.k_out + bh * g.cap * vpr;
   uint4* vout = g.v_out + bh * g.cap * vpr;
   const int n_win = (g.l_obs - (int)rank + (int)csize - 1) / (int)csize;   // window rows of this CTA
@@ -454,7 +454,7 @@ cudaError_t launch_pool_topk(const CompressJob& job, bool* gathered) {
     g.k_out = static_cast<uint4*>(job.k_out);
     g.v_out = static_cast<uint4*>(job.v_out);
     g.len_out = job.len_out;
-    g.l_prompt = job.l_prompt;
+    g.kv_stride = job.kv_stride;
     g.cap = job.cap;
     g.vpr = job.head_dim * (job.dtype == SNAPKV_BF16 ? 2 : 4) / 16;
     g.l_obs = job.l_obs;

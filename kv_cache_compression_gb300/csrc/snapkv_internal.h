@@ -12,6 +12,7 @@ struct CompressJob {
   int batch, heads, head_dim, l_obs, pool_kernel, scope, dtype;
   int q_rows;          // window-query rows per KV head: (query heads / KV heads) * l_obs
   int64_t l_prompt, l_prefix, k_sel, cap;
+  int64_t kv_stride;   // rows between heads in k and v (>= l_prompt; larger for padded varlen batches)
   const void* q_obs;
   const void* k;
   const void* v;

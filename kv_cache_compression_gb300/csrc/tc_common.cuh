@@ -66,11 +66,14 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-inline bool make_map(CUtensorMap* map, const void* ptr, int d, int64_t rows, int64_t heads, int box_rows) {
+// `stride_rows` (>= rows) is the distance between heads in rows (0: rows).
+inline bool make_map(CUtensorMap* map, const void* ptr, int d, int64_t rows, int64_t heads, int box_rows,
+                     int64_t stride_rows = 0) {
+  if (stride_rows <= 0) stride_rows = rows;
   auto enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
-  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)stride_rows * d * 2};
   const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,

@@ -411,7 +411,7 @@ cudaError_t launch_cluster_typed(const CompressJob& job) {
   if (cluster_smem_ready<D, N, GQ>() < 0) return cudaErrorInvalidConfiguration;
   CUtensorMap mk, mq;
   const int64_t bh = (int64_t)job.batch * job.heads;
-  if (!tc::make_map(&mk, job.k, D, job.l_prompt, bh, kTileKeys) ||
+  if (!tc::make_map(&mk, job.k, D, job.l_prompt, bh, kTileKeys, job.kv_stride) ||
       !tc::make_map(&mq, job.q_obs, D, job.q_rows, bh, N))
     return cudaErrorInvalidValue;
   ClArgs a;

@@ -26,7 +26,7 @@ struct VoteParams {
   const void* k;
   float* partial;       // [B*H][n_chunk_all][rows][2] (m, z)
   float* c_out;         // [B*H][l_prefix]
-  int64_t l_prompt, l_prefix;
+  int64_t l_prompt, l_prefix, kv_stride;
   int l_obs, rows, scope, chunk, n_chunk_all;   // rows: window-query rows per head
   float scale_log2;     // log2(e) / sqrt(d)
 };
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kThreads) vote_simt_kernel(VoteParams a, int p
   const int64_t col0 = (int64_t)blockIdx.x * a.chunk;
   const int64_t col1 = min(col0 + (int64_t)a.chunk, pass == 0 ? a.l_prompt : a.l_prefix);
   const T* qg = static_cast<const T*>(a.q_obs) + bh * a.rows * D;
-  const T* kg = static_cast<const T*>(a.k) + bh * a.l_prompt * D;
+  const T* kg = static_cast<const T*>(a.k) + bh * a.kv_stride * D;
 
   for (int i = tid; i < LQ; i += kThreads) row_pos[i] = i % a.l_obs;
   for (int u = tid; u < LQ * VPR; u += kThreads) {
@@ -236,6 +236,7 @@ cudaError_t launch_vote_simt(const CompressJob& job) {
   a.partial = job.partial;
   a.c_out = job.c;
   a.l_prompt = job.l_prompt;
+  a.kv_stride = job.kv_stride;
   a.l_prefix = job.l_prefix;
   a.l_obs = job.l_obs;
   a.rows = job.q_rows;

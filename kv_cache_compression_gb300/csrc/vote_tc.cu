@@ -557,7 +557,7 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   const int group = job.q_rows / job.l_obs;                 // query heads per KV head
   const int64_t bh_kv = (int64_t)job.batch * job.heads;
   const int64_t bh = bh_kv * group;                           // query heads: the kernel's heads
-  if (!tc::make_map(&mk, job.k, D, job.l_prompt, bh_kv, kTileKeys) ||
+  if (!tc::make_map(&mk, job.k, D, job.l_prompt, bh_kv, kTileKeys, job.kv_stride) ||
       !tc::make_map(&mq, job.q_obs, D, job.l_obs, bh, N))
     return cudaErrorInvalidValue;
   TcArgs a;

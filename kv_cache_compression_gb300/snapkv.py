@@ -80,6 +80,10 @@ def lib():
         L.snapkv_compress_gqa_workspace_size.argtypes = [PP, I32]
         L.snapkv_compress_gqa.restype = I32
         L.snapkv_compress_gqa.argtypes = [PP, I32, P, P, P, P, P, I64, P, P, P, P, SZ, P, P]
+        L.snapkv_compress_varlen_workspace_size.restype = SZ
+        L.snapkv_compress_varlen_workspace_size.argtypes = [PP, P]
+        L.snapkv_compress_varlen.restype = I32
+        L.snapkv_compress_varlen.argtypes = [PP, P, P, P, P, P, P, I64, P, P, P, P, SZ, P, P]
         L.snapkv_hit_rate.restype = I32
         L.snapkv_hit_rate.argtypes = [P, P, I64, P, I64, P, I64, I32, I32, I32, I32, ctypes.c_double, P, P, P, P]
         L.snapkv_status_string.restype = ctypes.c_char_p
@@ -198,6 +202,60 @@ def compress(q_obs, k, v, *, pool_kernel, ratio_p=0.0, budget=0, scope="prompt_c
         raise SnapKVError(st, "snapkv_compress" if q_heads == H else "snapkv_compress_gqa")
     return {"k_out": k_out, "v_out": v_out, "len": len_out, "idx": idx_out, "vote": vote_out, "k": ksel,
             "workspace": workspace, "cap": cap}
+
+
+def compress_varlen(q_obs, k, v, l_prompts, *, pool_kernel, ratio_p=0.0, budget=0, scope="prompt_causal",
+                    algo="auto", cap=None, want_idx=True, want_vote=False, workspace=None, dev_status=None,
+                    stream=None, out=None):
+    """snapkv_compress_varlen: q_obs [B,H,L_obs,d]; k, v [B,H,L_max,d] padded, sequence b using its
+    first l_prompts[b] rows. Returns k_out, v_out [B,H,cap,d], len [B], idx [B,H,k_max] (row b, h
+    holds k_b indices), vote [B,H,L_max-L_obs] (if wanted), ks (per-sequence k) and the workspace.
+    ``out``: a previous call's result whose buffers (outputs and workspace) this call writes again."""
+    import numpy as np
+    import torch
+    B, H, L, d = k.shape
+    l_obs = q_obs.shape[2]
+    lens = np.ascontiguousarray(np.asarray(l_prompts, dtype=np.int64))
+    if lens.shape != (B,):
+        raise ValueError("one prompt length per sequence")
+    params = make_params(batch=B, heads=H, head_dim=d, l_obs=l_obs, l_prompt=L, pool_kernel=pool_kernel,
+                         ratio_p=ratio_p, budget=budget, scope=scope, dtype=_dtype_code(k), algo=algo)
+    k_max = kept(params)
+    ks = []
+    for n in lens:
+        pb = make_params(batch=1, heads=H, head_dim=d, l_obs=l_obs, l_prompt=int(n), pool_kernel=pool_kernel,
+                         ratio_p=ratio_p, budget=budget, scope=scope, dtype=_dtype_code(k), algo=algo)
+        ks.append(kept(pb))
+    dev = k.device
+    if out is not None:
+        cap, k_out, v_out, len_out, idx_out, vote_out = (out["cap"], out["k_out"], out["v_out"], out["len"],
+                                                        out["idx"], out["vote"])
+        workspace = out["workspace"] if workspace is None else workspace
+    else:
+        if cap is None:
+            cap = k_max + l_obs
+        k_out = torch.empty((B, H, cap, d), dtype=k.dtype, device=dev)
+        v_out = torch.empty_like(k_out)
+        len_out = torch.empty((B,), dtype=torch.int32, device=dev)
+        idx_out = torch.full((B, H, max(k_max, 1)), -1, dtype=torch.int32, device=dev) if want_idx else None
+        vote_out = torch.zeros((B, H, L - l_obs), dtype=torch.float32, device=dev) if want_vote else None
+    need = int(lib().snapkv_compress_varlen_workspace_size(ctypes.byref(params), lens.ctypes.data_as(ctypes.c_void_p)))
+    if need == 0:
+        raise SnapKVError(ERR_INVALID_ARG, "snapkv_compress_varlen_workspace_size")
+    if workspace is None:
+        workspace = new_workspace(need, dev)
+    for t in (q_obs, k, v):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    st = lib().snapkv_compress_varlen(ctypes.byref(params), lens.ctypes.data_as(ctypes.c_void_p), _ptr(q_obs),
+                                      _ptr(k), _ptr(v), _ptr(k_out), _ptr(v_out), int(cap), _ptr(len_out),
+                                      _ptr(idx_out), _ptr(vote_out), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                                      _stream_handle(stream))
+    if st != OK:
+        raise SnapKVError(st, "snapkv_compress_varlen")
+    return {"k_out": k_out, "v_out": v_out, "len": len_out, "idx": idx_out, "vote": vote_out, "ks": ks,
+            "k_max": k_max, "workspace": workspace, "cap": cap}
 
 
 def append(k_new, v_new, k_cache, v_cache, len_, *, dev_status=None, stream=None):

@@ -312,6 +312,28 @@ def device_inputs(wl: Workload, layer: int, seq0: int, nseq: int, l_prompt: int,
     return q, k, v, plants
 
 
+def device_inputs_padded(wl: Workload, layer: int, seq0: int, lengths, device, l_pad: Optional[int] = None,
+                         pad_value: float = float("nan"), stream=0):
+    """Ragged prompts in one padded batch: q_obs [n,H,L_obs,d] and k, v [n,H,L_pad,d] where sequence
+    seq0+b holds its own prompt (length lengths[b], identical to ``device_inputs`` of that sequence
+    alone) in rows [0, lengths[b]) and ``pad_value`` in the rows after it."""
+    import torch
+    n = len(lengths)
+    L_pad = l_pad if l_pad is not None else max(lengths)
+    H, d, lo = wl.heads, wl.head_dim, wl.l_obs
+    dt = torch.bfloat16 if wl.bf16 else torch.float32
+    q = torch.empty((n, H, lo, d), dtype=dt, device=device)
+    k = torch.full((n, H, L_pad, d), pad_value, dtype=dt, device=device)
+    v = torch.full((n, H, L_pad, d), pad_value, dtype=dt, device=device)
+    for b, L in enumerate(lengths):
+        qb, kb, vb, _ = device_inputs(wl, layer, seq0 + b, 1, int(L), device, stream=stream)
+        q[b].copy_(qb[0])
+        k[b, :, :L].copy_(kb[0])
+        v[b, :, :L].copy_(vb[0])
+        del qb, kb, vb
+    return q, k, v
+
+
 def host_decode_token(wl: Workload, layer: int, seq: int, head: int, step: int):
     """(q, k, v) of decode step ``step`` for one head, as fp32 values [d]."""
     out = []

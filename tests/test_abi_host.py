@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = sk.declared_functions()
-    assert len(names) == 13
+    assert len(names) == 15
     for n in names:
         assert hasattr(lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", sk.library_path()], capture_output=True, text=True).stdout
@@ -112,6 +112,26 @@ def test_gqa_rejects_bad_groupings(lib):
     assert lib.snapkv_compress_gqa(ctypes.byref(p), 6, *args) == sk.ERR_INVALID_ARG
     assert lib.snapkv_compress_gqa(ctypes.byref(p), 2, *args) == sk.ERR_INVALID_ARG   # fewer query heads
     assert lib.snapkv_compress_gqa(ctypes.byref(p), 20, *args) == sk.ERR_UNSUPPORTED
+
+
+def test_varlen_workspace_and_validation(lib):
+    import numpy as np
+    P = ctypes.c_void_p
+    p = _params(heads=2, l_prompt=1024)
+    ok = np.array([1024, 200, 600], dtype=np.int64)
+    p.batch = 3
+    size = lib.snapkv_compress_varlen_workspace_size(ctypes.byref(p), ok.ctypes.data_as(P))
+    full = sk.compress_workspace_size(_params(heads=2, l_prompt=1024, batch=1))
+    assert size == full                                  # the longest sequence needs the most
+    for bad in ([1025, 200, 600], [32, 200, 600], [0, 200, 600]):   # longer than the padding, <= L_obs
+        b = np.array(bad, dtype=np.int64)
+        assert lib.snapkv_compress_varlen_workspace_size(ctypes.byref(p), b.ctypes.data_as(P)) == 0
+        assert lib.snapkv_compress_varlen(ctypes.byref(p), b.ctypes.data_as(P), P(16), P(32), P(48), P(64), P(80),
+                                          100, P(96), None, None, P(256), 1 << 30, None, None) == sk.ERR_INVALID_ARG
+    # cap must hold the longest sequence's k + L_obs
+    assert lib.snapkv_compress_varlen(ctypes.byref(p), ok.ctypes.data_as(P), P(16), P(32), P(48), P(64), P(80),
+                                      sk.kept(p) + 31, P(96), None, None, P(256), 1 << 30, None, None) \
+        == sk.ERR_CAPACITY
 
 
 def test_hit_rate_rejects_bad_arguments(lib):

@@ -68,6 +68,8 @@ def lib():
         L.snapkv_compress_workspace_size.argtypes = [PP]
         L.snapkv_compress.restype = I32
         L.snapkv_compress.argtypes = [PP, P, P, P, P, P, I64, P, P, P, P, SZ, P, P]
+        L.snapkv_compress_profiled.restype = I32
+        L.snapkv_compress_profiled.argtypes = [PP, P, P, P, P, P, I64, P, P, P, P, SZ, P, P, P, I32]
         L.snapkv_append.restype = I32
         L.snapkv_append.argtypes = [P, P, P, P, I64, P, I32, I32, I32, I32, P, P]
         L.snapkv_decode_workspace_size.restype = SZ

@@ -48,6 +48,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the measurements after the timed region (full-cache decode, hit rate, GQA, varlen); "
+                         "used for profiler captures of the step alone")
     return ap.parse_args()
 
 
@@ -671,10 +674,11 @@ def run_ours(args, rank, world, local_rank):
 
     if rank != 0:
         return
-    full_cache = full_cache_decode(torch, snapkv, synth, dev) if world == 1 else None
-    hit = hit_rate_diagnostic(torch, snapkv, synth, dev, *copies[0], wl) if world == 1 else None
-    gqa = gqa_compress(torch, snapkv, synth, dev) if world == 1 else None
-    varlen = varlen_compress(torch, snapkv, synth, dev) if world == 1 else None
+    extras = world == 1 and not args.no_extras
+    full_cache = full_cache_decode(torch, snapkv, synth, dev) if extras else None
+    hit = hit_rate_diagnostic(torch, snapkv, synth, dev, *copies[0], wl) if extras else None
+    gqa = gqa_compress(torch, snapkv, synth, dev) if extras else None
+    varlen = varlen_compress(torch, snapkv, synth, dev) if extras else None
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline()

@@ -36,23 +36,44 @@ __global__ void __launch_bounds__(256)
 append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, uint4* __restrict__ k_cache,
               uint4* __restrict__ v_cache, int64_t cap, int32_t* __restrict__ len, int heads, int vpr,
               int32_t* __restrict__ dev_status) {
-  __shared__ int pos;
   const int b = blockIdx.x;
+  // The new rows and the length are loaded together (one memory round trip): every thread reads
+  // len[b] itself; the barrier below keeps the update after every thread's read.
+  constexpr int kPer = 4;   // 16-byte pieces of K (and of V) per thread per round
+  const int total = heads * vpr;
+  const int64_t row0 = (int64_t)b * heads * vpr;
+  const int p = len[b];
+  const bool ok = p >= 0 && (int64_t)p < cap;
+  for (int base = 0; base < total; base += kPer * (int)blockDim.x) {
+    uint4 kv[kPer], vv[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int u = base + i * (int)blockDim.x + (int)threadIdx.x;
+      if (u < total) {
+        kv[i] = k_new[row0 + u];
+        vv[i] = v_new[row0 + u];
+      }
+    }
+    if (ok) {
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int u = base + i * (int)blockDim.x + (int)threadIdx.x;
+        if (u < total) {
+          const int h = u / vpr, c = u % vpr;
+          const int64_t bh = (int64_t)b * heads + h;
+          k_cache[(bh * cap + p) * vpr + c] = kv[i];
+          v_cache[(bh * cap + p) * vpr + c] = vv[i];
+        }
+      }
+    }
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    const int p = len[b];
-    pos = (p >= 0 && (int64_t)p < cap) ? p : -1;
-    if (pos < 0) report(dev_status, SNAPKV_ERR_CAPACITY);
+    if (ok)
+      len[b] = p + 1;
+    else
+      report(dev_status, SNAPKV_ERR_CAPACITY);
   }
-  __syncthreads();
-  if (pos < 0) return;
-  for (int u = threadIdx.x; u < heads * vpr; u += blockDim.x) {
-    const int h = u / vpr, c = u % vpr;
-    const int64_t bh = (int64_t)b * heads + h;
-    k_cache[(bh * cap + pos) * vpr + c] = k_new[bh * vpr + c];
-    v_cache[(bh * cap + pos) * vpr + c] = v_new[bh * vpr + c];
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) len[b] = pos + 1;
 }
 
 struct DecArgs {

@@ -195,3 +195,46 @@ def test_device_generator_matches_host(dev):
     assert np.array_equal(to_numpy_f32(k[0, 7]), hi.k)
     assert np.array_equal(to_numpy_f32(v[0, 7]), hi.v)
     assert np.array_equal(to_numpy_f32(q[0, 7]), hi.q_obs)
+
+
+@pytest.mark.parametrize("algo", ["auto", "simt"])
+def test_zero_queries_short_prefix(dev, algo):
+    """Every pooled score equal on a prefix short enough for the top-k to gather all of them as
+    candidates: ties still go to the lower index."""
+    from kv_cache_compression_gb300 import snapkv
+    B, H, L, lo, d = 1, 2, 2000, 32, 128
+    k = torch.randn(B, H, L, d, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).to(dev)
+    q = torch.zeros(B, H, lo, d, dtype=torch.bfloat16, device=dev)
+    res = snapkv.compress(q, k, k.clone(), pool_kernel=7, budget=500, algo=algo)
+    torch.cuda.synchronize()
+    for h in range(H):
+        assert res["idx"][0, h].cpu().tolist() == list(range(500))
+
+
+@pytest.mark.parametrize("algo", ["auto", "tensor_core_cluster", "simt"])
+def test_tied_block_cut_across_slices(dev, algo):
+    """A block of zero keys gets one exactly tied vote; the budget cuts inside the block so that the
+    kept copies (lowest index first) run past the boundary between two CTAs' slices of the top-k."""
+    from kv_cache_compression_gb300 import snapkv
+    L, lo, d = 4032, 32, 128
+    g = torch.Generator().manual_seed(7)
+    q = torch.randn(1, 1, lo, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, 1, L, d, generator=g)
+    k[:, :, 1000:2500] = 0.0
+    k = k.to(torch.bfloat16)
+    v = torch.randn(1, 1, L, d, generator=g).to(torch.bfloat16)
+    qf, kf, vf = (to_numpy_f32(t[0, 0]) for t in (q, k, v))
+    l_prefix = L - lo
+    c = orc.vote(qf, kf)
+    p = orc.max_pool(c, 7)
+    tie = p[1500]                                        # inside the block, away from its edges
+    assert np.sum(p == tie) > 1300
+    budget = int(np.sum(p > tie)) + 1200
+    ref = orc.compress_head(qf, kf, vf, pool_kernel=7, budget=budget)
+    res = snapkv.compress(q.to(dev), k.to(dev), v.to(dev), pool_kernel=7, budget=budget, algo=algo, want_vote=True)
+    torch.cuda.synchronize()
+    check_compress_head(gpu_idx=res["idx"][0, 0].cpu().numpy(), gpu_kc=to_numpy_f32(res["k_out"][0, 0]),
+                        gpu_vc=to_numpy_f32(res["v_out"][0, 0]), gpu_vote=res["vote"][0, 0].cpu().numpy(), ref=ref,
+                        k_in=kf, v_in=vf, l_prefix=l_prefix, l_obs=lo, where="tied block")
+    kept_ties = np.intersect1d(res["idx"][0, 0].cpu().numpy(), np.nonzero(p == tie)[0])
+    assert kept_ties.size == budget - int(np.sum(p > tie)) and kept_ties[-1] > 2000   # past the first slice

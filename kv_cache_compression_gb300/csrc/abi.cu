@@ -4,6 +4,8 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <vector>
+
 #include "snapkv_common.cuh"
 #include "snapkv_internal.h"
 
@@ -267,7 +269,11 @@ size_t snapkv_compress_varlen_workspace_size(const snapkv_compress_params* param
     const size_t t = compress_layout(1, pb.heads, pb.l_obs, rows, pb.l_prompt, k).total;
     if (t > need) need = t;
   }
-  return need;
+  // One launch over the whole batch lays the batch out with the longest sequence's sizes.
+  int64_t lp_max = 0, k_max = 0;
+  check_params(params, params->heads, &lp_max, &k_max, &rows);
+  const size_t all = compress_layout(params->batch, params->heads, params->l_obs, rows, params->l_prompt, k_max).total;
+  return all > need ? all : need;
 }
 
 snapkv_status snapkv_compress_varlen(const snapkv_compress_params* params, const int64_t* l_prompts,
@@ -301,6 +307,67 @@ snapkv_status snapkv_compress_varlen(const snapkv_compress_params* params, const
 
   const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
+
+  // The whole ragged batch in one launch of the score/vote kernel and one of the top-k kernel,
+  // when the tensor-core path takes it (every sequence keeps at least one row, and the longest
+  // fits the resident queue); otherwise one compression per sequence, one after another.
+  std::vector<int64_t> ks((size_t)params->batch);
+  for (int32_t b = 0; b < params->batch; ++b) {
+    snapkv_compress_params pb = *params;
+    pb.batch = 1;
+    pb.l_prompt = l_prompts[b];
+    int64_t lpb = 0;
+    int rows_b = 0;
+    check_params(&pb, pb.heads, &lpb, &ks[(size_t)b], &rows_b);   // validated above
+  }
+  if (params->algo == SNAPKV_ALGO_AUTO || params->algo == SNAPKV_ALGO_TENSOR_CORE) {
+    const CompressLayout L = compress_layout(params->batch, params->heads, params->l_obs, rows, params->l_prompt, k_max);
+    CompressJob job;
+    job.batch = params->batch;
+    job.heads = params->heads;
+    job.head_dim = params->head_dim;
+    job.l_obs = params->l_obs;
+    job.q_rows = rows;
+    job.pool_kernel = params->pool_kernel;
+    job.scope = params->softmax_scope;
+    job.dtype = params->dtype;
+    job.l_prompt = params->l_prompt;
+    job.kv_stride = params->l_prompt;
+    job.l_prefix = lp_max;
+    job.k_sel = k_max;
+    job.cap = cap;
+    job.q_obs = q_obs;
+    job.k = k;
+    job.v = v;
+    job.k_out = k_out;
+    job.v_out = v_out;
+    job.len_out = len_out;
+    job.idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
+    job.c = vote_out ? vote_out : reinterpret_cast<float*>(ws + L.c);
+    job.p = reinterpret_cast<float*>(ws + L.p);
+    job.partial = reinterpret_cast<float*>(ws + L.partial);
+    job.c_q = reinterpret_cast<float*>(ws + L.c_q);
+    job.tc_zsum = reinterpret_cast<double*>(ws + L.tc_zsum);
+    job.tc_cnt = reinterpret_cast<uint32_t*>(ws + L.tc_counters);
+    job.tc_zero_bytes = L.total - L.tc_zsum;
+    job.vote_chunk = L.vote_chunk;
+    job.n_chunk_all = L.n_chunk_all;
+    job.n_chunk_prefix = L.n_chunk_prefix;
+    job.dev_status = dev_status;
+    job.stream = strm;
+    job.events = nullptr;
+    job.n_events = 0;
+    job.n_var = params->batch;
+    job.var_l_prompt = l_prompts;
+    job.var_k = ks.data();
+    if (vote_tc_ragged_eligible(job) && pool_topk_ragged_eligible(job)) {
+      if (launch_vote_tc(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
+      bool gathered = false;
+      if (launch_pool_topk(job, &gathered) != cudaSuccess || !gathered) return SNAPKV_ERR_CUDA;
+      return SNAPKV_OK;
+    }
+  }
+
   for (int32_t b = 0; b < params->batch; ++b) {
     snapkv_compress_params pb = *params;
     pb.batch = 1;

@@ -223,7 +223,15 @@ struct GatherArgs {
   uint4* v_out;
   int32_t* len_out;
   int64_t kv_stride, cap;   // rows between heads in k / v, rows per head in k_out / v_out
+  int64_t c_stride, idx_stride;   // rows between heads in the vote and in the indices
   int vpr, l_obs, heads;
+  // Ragged batch (n > 0): sequence s (= head / heads) has its own prefix length and kept count;
+  // the kernel's l_prefix, k_sel and slice arguments are then the maxima.
+  struct {
+    int n;
+    int l_prefix[kMaxVarSeq];
+    int k[kMaxVarSeq];
+  } var;
 };
 
 __global__ void __launch_bounds__(kCThreads)
@@ -235,6 +243,7 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   float* cbuf = reinterpret_cast<float*>(work);              // [slice + 2 * radius] vote with halo
   uint32_t* hist = work;                                     // [kMaxBins] this slice's histogram
   uint32_t* sums = work + round4(max(slice + 2 * radius, kHistWords));   // [2][kMaxBins] cluster histograms
+  // (the layout above is sized for the largest slice; a ragged batch's shorter sequences use less)
   uint32_t* sh_warp = sums + kSumWords;                      // [32]
   uint32_t* counts = sh_warp + 32;                           // [8 + 1] packed (greater << 16 | equal) per slice
   __shared__ uint32_t sh_digit, sh_above, sh_full;
@@ -242,8 +251,14 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t rank = ptx::cluster_rank(), csize = ptx::cluster_size();
   const int64_t bh = blockIdx.x / csize;
-  const float* c = c_all + bh * l_prefix;
-  int32_t* idx = idx_all + bh * k_sel;
+  if (g.var.n > 0) {   // this head's sequence of a ragged batch
+    const int sq = (int)(bh / g.heads);
+    l_prefix = g.var.l_prefix[sq];
+    k_sel = g.var.k[sq];
+    slice = (int)((l_prefix + (int64_t)csize - 1) / (int64_t)csize);
+  }
+  const float* c = c_all + bh * g.c_stride;
+  int32_t* idx = idx_all + bh * g.idx_stride;
   const int L = (int)l_prefix;
   const int j0 = min(L, (int)rank * slice), j1 = min(L, j0 + slice);
   const int n = j1 - j0;
@@ -418,6 +433,14 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
 
 }  // namespace
 
+bool pool_topk_ragged_eligible(const CompressJob& job) {
+  if (job.n_var < 1 || job.n_var > kMaxVarSeq) return false;
+  if (!(job.l_prefix <= kClusterMaxPrefix && job.pool_kernel <= 1025)) return false;
+  for (int b = 0; b < job.n_var; ++b)
+    if (job.var_k[b] < 1) return false;
+  return true;
+}
+
 cudaError_t launch_pool_topk(const CompressJob& job, bool* gathered) {
   const int64_t bh = (int64_t)job.batch * job.heads;
   if (gathered) *gathered = false;
@@ -425,6 +448,8 @@ cudaError_t launch_pool_topk(const CompressJob& job, bool* gathered) {
   cudaError_t err = cudaSuccess;
   if (job.k_sel <= 0) {
     // Nothing is selected: no launch.
+  } else if (job.n_var > 0 && !(job.l_prefix <= kClusterMaxPrefix && job.pool_kernel <= 1025)) {
+    err = cudaErrorInvalidValue;   // a ragged batch takes the cluster kernel only
   } else if (job.l_prefix <= kClusterMaxPrefix && job.pool_kernel <= 1025) {
     int cl = (int)((job.l_prefix + 2047) / 2048);
     if (cl > kMaxCluster) cl = kMaxCluster;
@@ -459,6 +484,18 @@ cudaError_t launch_pool_topk(const CompressJob& job, bool* gathered) {
     g.vpr = job.head_dim * (job.dtype == SNAPKV_BF16 ? 2 : 4) / 16;
     g.l_obs = job.l_obs;
     g.heads = job.heads;
+    g.c_stride = job.l_prefix;
+    g.idx_stride = job.k_sel;
+    g.var.n = 0;
+    if (job.n_var > 0) {
+      if (job.n_var > kMaxVarSeq) return cudaErrorInvalidValue;
+      g.var.n = job.n_var;
+      for (int b = 0; b < job.n_var; ++b) {
+        g.var.l_prefix[b] = (int)(job.var_l_prompt[b] - job.l_obs);
+        g.var.k[b] = (int)job.var_k[b];
+        if (g.var.k[b] < 1) return cudaErrorInvalidValue;   // a ragged launch keeps at least one row
+      }
+    }
     err = cudaLaunchKernelEx(&cfg, pool_topk_cluster_kernel, (const float*)job.c, job.idx, job.l_prefix,
                              job.pool_kernel / 2, job.k_sel, slice, g);
     if (gathered) *gathered = err == cudaSuccess;

@@ -7,12 +7,21 @@
 
 namespace snapkv {
 
+// Sequences of a ragged batch that the score/vote and top-k kernels take in one launch.
+constexpr int kMaxVarSeq = 64;
+
 // One compression call, after host-side validation.
 struct CompressJob {
   int batch, heads, head_dim, l_obs, pool_kernel, scope, dtype;
   int q_rows;          // window-query rows per KV head: (query heads / KV heads) * l_obs
   int64_t l_prompt, l_prefix, k_sel, cap;
   int64_t kv_stride;   // rows between heads in k and v (>= l_prompt; larger for padded varlen batches)
+  // Ragged batch in one launch (n_var > 0, at most kMaxVarSeq): sequence b has var_l_prompt[b]
+  // prompt rows and keeps var_k[b] prefix rows; l_prompt, l_prefix and k_sel then hold the maxima,
+  // which are also the row strides of the vote (c) and of the indices (idx).
+  int n_var = 0;
+  const int64_t* var_l_prompt = nullptr;   // host array [batch]
+  const int64_t* var_k = nullptr;          // host array [batch]
   const void* q_obs;
   const void* k;
   const void* v;
@@ -65,6 +74,10 @@ bool vote_cluster_eligible(const CompressJob& job);
 cudaError_t launch_vote_cluster(const CompressJob& job);
 int vote_tc_keys_per_item(int q_rows, int l_obs);
 cudaError_t launch_vote_tc(const CompressJob& job);
+// Whether a ragged batch (job.n_var > 0, maxima in l_prompt / l_prefix / k_sel) can take one
+// launch of the score/vote kernel and one of the cluster top-k kernel.
+bool vote_tc_ragged_eligible(const CompressJob& job);
+bool pool_topk_ragged_eligible(const CompressJob& job);
 // Max-pool + top-k; for prefixes the cluster kernel handles it also writes K_c, V_c and len_out
 // (*gathered = true), otherwise launch_gather must follow.
 cudaError_t launch_pool_topk(const CompressJob& job, bool* gathered);

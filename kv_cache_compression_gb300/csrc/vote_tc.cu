@@ -59,31 +59,69 @@ constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clock
 constexpr long long kDrainLimit = 400000000LL;
 
+// Per-sequence sizes of a ragged batch: the queue holds the sequences one after another, heads in
+// order within a sequence, key chunks in order within a head.
+struct VarSeqs {
+  int n;                          // sequences (0: a uniform batch)
+  int heads;                      // heads per sequence
+  int item0[kMaxVarSeq + 1];      // first queue position of each sequence
+  int n_chunk[kMaxVarSeq];
+  int64_t l_prompt[kMaxVarSeq];
+};
+
 struct TcArgs {
-  int64_t l_prompt, l_prefix;
+  int64_t l_prompt, l_prefix;     // uniform batch (ragged: the maxima)
+  int64_t c_stride;               // row stride of c_out (l_prefix, or its maximum for a ragged batch)
   int l_obs, scope, n_chunk, n_queue, keys_per_item, bh_total, delta;
   int group;         // query heads per KV head: head h reads the keys of KV head h / group
   int resident;      // 1: one item per key chunk, logits stay in TMEM from statistics to vote
   float scale_log2;
   double* zsum;      // [BH][l_obs]: Z_i = sum_j 2^(s'_ij) over the head's visible keys (fp64)
   uint32_t* cnt;     // [BH] A items whose contribution to zsum is complete
-  float* c_out;      // [BH][l_prefix]
+  float* c_out;      // [BH][c_stride]
   int32_t* dev_status;
 };
+
+// Kernel parameters: a ragged batch carries its per-sequence sizes, a uniform one nothing more.
+template <bool VAR>
+struct TcParams : TcArgs {
+  VarSeqs vs;
+};
+template <>
+struct TcParams<false> : TcArgs {};
 
 struct Item {
   int kind;   // 0: statistics (A), 1: vote (B)
   int head;
   int chunk;
+  int l_prompt;        // the head's prompt length
 };
 
 // Queue position -> item. Blocks of n_chunk positions: A(0..delta-1), then B(h), A(h + delta)
 // alternating, then the last B heads.
-__device__ __forceinline__ Item queue_item(const TcArgs& a, int p) {
+template <bool VAR>
+__device__ __forceinline__ Item queue_item(const TcParams<VAR>& a, int p) {
+  Item it;
+  if constexpr (VAR) {   // ragged batch (resident mode only)
+    int lo = 0, hi = a.vs.n - 1;   // the sequence s with item0[s] <= p < item0[s + 1]
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.vs.item0[mid] <= p)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int local = p - a.vs.item0[lo], nc = a.vs.n_chunk[lo];
+    it.kind = 0;
+    it.head = lo * a.vs.heads + local / nc;
+    it.chunk = local % nc;
+    it.l_prompt = (int)a.vs.l_prompt[lo];
+    return it;
+  }
   const int nc = a.n_chunk, H = a.bh_total, D = a.delta;
   const int blk = p / nc, off = p % nc;
-  Item it;
   it.chunk = off;
+  it.l_prompt = (int)a.l_prompt;
   if (a.resident) {   // every item is a statistics item whose vote follows from TMEM
     it.kind = 0;
     it.head = blk;
@@ -157,16 +195,27 @@ __device__ __forceinline__ void fail(const Ctx& c, int32_t* dev_status) {
   *c.abort = 1;
 }
 
-__device__ __forceinline__ int tiles_of(const TcArgs& a, int chunk, int TI) {
-  const int64_t key0 = (int64_t)chunk * a.keys_per_item;
-  const int64_t left = a.l_prompt - key0;
+// Prompt length of an item's head: per item in a ragged batch, else the batch's.
+template <bool VAR>
+__device__ __forceinline__ int64_t prompt_of(const TcArgs& a, const Item& it) {
+  if constexpr (VAR)
+    return (int64_t)it.l_prompt;
+  else
+    return a.l_prompt;
+}
+
+template <bool VAR>
+__device__ __forceinline__ int tiles_of(const TcArgs& a, const Item& it, int TI) {
+  const int64_t key0 = (int64_t)it.chunk * a.keys_per_item;
+  const int64_t left = prompt_of<VAR>(a, it) - key0;
   const int t = (int)((left + kTileKeys - 1) / kTileKeys);
   return t < TI ? t : TI;
 }
 
-template <int D, int N>
+template <int D, int N, bool VAR>
 __global__ void __launch_bounds__(kThreadsTc, 1)
-vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q, TcArgs a) {
+vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+               TcParams<VAR> a) {
   using Lay = TcLayout<D, N>;
   constexpr int TI = Lay::TI;
   extern __shared__ uint8_t smem_raw[];
@@ -215,7 +264,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       for (;; ++n) {
         const int p = blockIdx.x + n * gridDim.x;
         if (p >= a.n_queue || *c.abort) break;
-        const Item it = queue_item(a, p);
+        const Item it = queue_item<VAR>(a, p);
         const int qb = n & 1;
         if (!ptx::mbar_wait(&c.q_empty[qb], ((n >> 1) & 1) ^ 1, c.abort, kWaitLimit)) {
           fail(c, a.dev_status);
@@ -226,7 +275,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         for (int kb = 0; kb < Lay::KB; ++kb)
           ptx::tma_load_3d(base + Lay::OFF_Q + qb * Lay::Q_BYTES + kb * Lay::QB_BYTES, &tmap_q, kb * 64, 0, it.head,
                            &c.q_full[qb]);
-        const int tiles = tiles_of(a, it.chunk, TI);
+        const int tiles = tiles_of<VAR>(a, it, TI);
         const int key0 = it.chunk * a.keys_per_item;
         // Keys are read once, except in re-read mode where a head's vote items read its keys again
         // from L2: only those statistics loads ask L2 to keep the lines. Marking the whole stream
@@ -267,7 +316,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       for (int n = 0;; ++n) {
         const int p = blockIdx.x + n * gridDim.x;
         if (p >= a.n_queue || *c.abort) break;
-        const Item it = queue_item(a, p);
+        const Item it = queue_item<VAR>(a, p);
         const int slot = n % kSlots, use = n / kSlots, qb = n & 1;
         if (!ptx::mbar_wait(&c.tmem_empty[slot], (use & 1) ^ 1, c.abort, kWaitLimit) ||
             !ptx::mbar_wait(&c.q_full[qb], (n >> 1) & 1, c.abort, kWaitLimit)) {
@@ -275,7 +324,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
           break;
         }
         ptx::tc_fence_after();
-        const int tiles = tiles_of(a, it.chunk, TI);
+        const int tiles = tiles_of<VAR>(a, it, TI);
         const uint32_t q_addr = ptx::smem_u32(base + Lay::OFF_Q + qb * Lay::Q_BYTES);
         bool ok = true;
         for (int t = 0; t < TI; ++t) {
@@ -360,9 +409,11 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     // the slot is released after the last TMEM read.
     auto item_stats = [&](int n, const Item& it) {
       const int slot = n % kSlots;
-      const int tiles = tiles_of(a, it.chunk, TI);
+      const int tiles = tiles_of<VAR>(a, it, TI);
       const int64_t item_key0 = (int64_t)it.chunk * a.keys_per_item;
-      const int64_t lim = a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? a.l_prefix : a.l_prefix - 1;
+      const int64_t l_prompt = prompt_of<VAR>(a, it);
+      const int64_t l_prefix = VAR ? l_prompt - a.l_obs : a.l_prefix;
+      const int64_t lim = a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? l_prefix : l_prefix - 1;
       wait_tiles(slot, n / kSlots);
 #pragma unroll 1
       for (int r0 = 0; r0 < N; r0 += R) {
@@ -373,7 +424,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
           float acc[R];
           load_rows((uint32_t)(slot * TI * N + t * N + r0), acc);
           const int64_t tkey0 = item_key0 + t * kTileKeys;
-          if (tkey0 + kTileKeys <= a.l_prefix) {
+          if (tkey0 + kTileKeys <= l_prefix) {
 #pragma unroll
             for (int i = 0; i < R; ++i) v[i] = fmaxf(v[i], acc[i]);
           } else {
@@ -381,7 +432,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
             for (int i = 0; i < R; ++i) {
               const int row = r0 + i;
-              const bool vis = row < a.l_obs && key < a.l_prompt &&
+              const bool vis = row < a.l_obs && key < l_prompt &&
                                (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + row : key <= lim);
               if (vis) v[i] = fmaxf(v[i], acc[i]);
             }
@@ -406,7 +457,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
           float acc[R];
           load_rows((uint32_t)(slot * TI * N + t * N + r0), acc);
           const int64_t tkey0 = item_key0 + t * kTileKeys;
-          if (tkey0 + kTileKeys <= a.l_prefix) {
+          if (tkey0 + kTileKeys <= l_prefix) {
 #pragma unroll
             for (int i = 0; i < R; ++i) v[i] += ex2(fmaf(acc[i], a.scale_log2, -mrow[i]));
           } else {
@@ -414,7 +465,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
             for (int i = 0; i < R; ++i) {
               const int row = r0 + i;
-              const bool vis = row < a.l_obs && key < a.l_prompt &&
+              const bool vis = row < a.l_obs && key < l_prompt &&
                                (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + row : key <= lim);
               if (vis) v[i] += ex2(fmaf(acc[i], a.scale_log2, -mrow[i]));
             }
@@ -453,10 +504,11 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     // C_j = sum_i 2^(s'_ij - c_i); the slot is released after the last TMEM read.
     auto item_vote = [&](int n, const Item& it) {
       const int slot = n % kSlots;
-      const int tiles = tiles_of(a, it.chunk, TI);
+      const int tiles = tiles_of<VAR>(a, it, TI);
       const int64_t item_key0 = (int64_t)it.chunk * a.keys_per_item;
       if (gtid == 0) {
-        const uint32_t need = (uint32_t)a.n_chunk;
+        const uint32_t need =
+            VAR ? (uint32_t)((it.l_prompt + a.keys_per_item - 1) / a.keys_per_item) : (uint32_t)a.n_chunk;
         if (ptx::ld_acquire_u32(a.cnt + it.head) < need) {
           const long long t0 = clock64();
           while (ptx::ld_acquire_u32(a.cnt + it.head) < need) {
@@ -495,7 +547,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
           for (int i = 0; i < R; ++i) csum += ex2(fmaf(acc[i], a.scale_log2, -cr[r0 + i]));
         }
-        if (key < a.l_prefix) a.c_out[(int64_t)it.head * a.l_prefix + key] = csum;
+        if (key < (VAR ? prompt_of<VAR>(a, it) - a.l_obs : a.l_prefix)) a.c_out[(int64_t)it.head * a.c_stride + key] = csum;
       }
       ptx::tc_fence_before();
       ptx::named_barrier(bar_id, 128);
@@ -510,7 +562,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       const int n = grp + 2 * k;
       const int p = blockIdx.x + n * gridDim.x;
       if (p >= a.n_queue || stop_uniform()) break;
-      const Item it = queue_item(a, p);
+      const Item it = queue_item<VAR>(a, p);
       if (it.kind == 0)
         item_stats(n, it);
       else
@@ -522,12 +574,12 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         // Otherwise the vote of the group's previous item, whose logits are still in TMEM, comes
         // after the statistics of this one (so no item of the CTA waits without its pass A).
         const int m = n - 2;
-        item_vote(m, queue_item(a, blockIdx.x + m * gridDim.x));
+        item_vote(m, queue_item<VAR>(a, blockIdx.x + m * gridDim.x));
       }
     }
     if (a.resident && !lag0 && k > 0 && !stop_uniform()) {
       const int m = grp + 2 * (k - 1);
-      item_vote(m, queue_item(a, blockIdx.x + m * gridDim.x));
+      item_vote(m, queue_item<VAR>(a, blockIdx.x + m * gridDim.x));
     }
   }
 
@@ -554,7 +606,6 @@ group_sum_kernel(const float* __restrict__ c_q, float* __restrict__ c, int64_t l
 template <int D, int N>
 cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   using Lay = TcLayout<D, N>;
-  auto kern = vote_tc_kernel<D, N>;
   if (grid <= 0) return cudaErrorInvalidConfiguration;   // tc_grid() also set the smem attribute
   cudaError_t err;
   CUtensorMap mk, mq;
@@ -567,6 +618,7 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   TcArgs a;
   a.l_prompt = job.l_prompt;
   a.l_prefix = job.l_prefix;
+  a.c_stride = job.l_prefix;
   a.l_obs = job.l_obs;
   a.group = group;
   a.scope = job.scope;
@@ -575,6 +627,23 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   a.bh_total = (int)bh;
   a.resident = a.n_chunk <= kSlots * grid ? 1 : 0;
   a.n_queue = (int)((a.resident ? 1 : 2) * bh * a.n_chunk);
+  TcParams<true> pv;
+  if (job.n_var > 0) {
+    // Ragged batch: n_chunk holds the largest head's items (the queue's deadlock-freedom
+    // conditions bound the items of a head), and the queue is resident only.
+    if (job.n_var > kMaxVarSeq || group != 1 || !a.resident) return cudaErrorInvalidValue;
+    pv.vs.n = job.n_var;
+    pv.vs.heads = job.heads;
+    int pos = 0;
+    for (int b = 0; b < job.n_var; ++b) {
+      pv.vs.item0[b] = pos;
+      pv.vs.l_prompt[b] = job.var_l_prompt[b];
+      pv.vs.n_chunk[b] = (int)((job.var_l_prompt[b] + a.keys_per_item - 1) / a.keys_per_item);
+      pos += job.heads * pv.vs.n_chunk[b];
+    }
+    pv.vs.item0[job.n_var] = pos;
+    a.n_queue = pos;
+  }
   // B items of a head come about four grids of queue positions after its last A item (so they
   // seldom wait), unless the keys read in between would no longer fit comfortably in L2.
   const int64_t want = 1 + (4 * (int64_t)grid + 2 * (int64_t)a.n_chunk - 1) / (2 * (int64_t)a.n_chunk);
@@ -604,7 +673,14 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   err = cudaMemsetAsync(job.tc_zsum, 0, job.tc_zero_bytes, job.stream);
   if (err != cudaSuccess) return err;
   job.mark(2 * kStageScore);
-  err = cudaLaunchKernelEx(&cfg, kern, mk, mq, a);
+  if (job.n_var > 0) {
+    static_cast<TcArgs&>(pv) = a;
+    err = cudaLaunchKernelEx(&cfg, vote_tc_kernel<D, N, true>, mk, mq, pv);
+  } else {
+    TcParams<false> pu;
+    static_cast<TcArgs&>(pu) = a;
+    err = cudaLaunchKernelEx(&cfg, vote_tc_kernel<D, N, false>, mk, mq, pu);
+  }
   job.mark(2 * kStageScore + 1);
   job.mark(2 * kStageVote);
   if (err == cudaSuccess && group > 1) {
@@ -634,9 +710,11 @@ int tc_grid() {
   int sms = 0, per_sm = 0;
   int grid = -1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-      cudaFuncSetAttribute(vote_tc_kernel<D, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES) ==
+      cudaFuncSetAttribute(vote_tc_kernel<D, N, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES) ==
           cudaSuccess &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vote_tc_kernel<D, N>, kThreadsTc, Lay::BYTES) ==
+      cudaFuncSetAttribute(vote_tc_kernel<D, N, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES) ==
+          cudaSuccess &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vote_tc_kernel<D, N, false>, kThreadsTc, Lay::BYTES) ==
           cudaSuccess &&
       per_sm > 0)
     grid = sms;
@@ -679,6 +757,17 @@ bool vote_tc_eligible(const CompressJob& job) {
   const int64_t n_chunk = (job.l_prompt + per_item - 1) / per_item;
   const int64_t q_heads = (int64_t)job.batch * job.heads * (job.q_rows / job.l_obs);
   return 2 * n_chunk * q_heads < ((int64_t)1 << 31);
+}
+
+// A ragged batch in one launch: resident mode for the longest sequence, at most kMaxVarSeq
+// sequences, no grouped query heads.
+bool vote_tc_ragged_eligible(const CompressJob& job) {
+  if (job.n_var < 1 || job.n_var > kMaxVarSeq || job.q_rows != job.l_obs || !vote_tc_eligible(job)) return false;
+  const int n = tc_n_pad<128>(job.l_obs);
+  const int grid = job.head_dim == 64 ? tc_grid_n<64>(n) : tc_grid_n<128>(n);
+  const int64_t per_item = vote_tc_keys_per_item(job.q_rows, job.l_obs);
+  const int64_t n_chunk = (job.l_prompt + per_item - 1) / per_item;
+  return n_chunk <= (int64_t)kSlots * grid;
 }
 
 cudaError_t launch_vote_tc(const CompressJob& job) {

@@ -121,8 +121,8 @@ def test_varlen_workspace_and_validation(lib):
     ok = np.array([1024, 200, 600], dtype=np.int64)
     p.batch = 3
     size = lib.snapkv_compress_varlen_workspace_size(ctypes.byref(p), ok.ctypes.data_as(P))
-    full = sk.compress_workspace_size(_params(heads=2, l_prompt=1024, batch=1))
-    assert size == full                                  # the longest sequence needs the most
+    full = sk.compress_workspace_size(_params(heads=2, l_prompt=1024, batch=3))
+    assert size == full            # one launch over the batch lays it out with the longest sequence's sizes
     for bad in ([1025, 200, 600], [32, 200, 600], [0, 200, 600]):   # longer than the padding, <= L_obs
         b = np.array(bad, dtype=np.int64)
         assert lib.snapkv_compress_varlen_workspace_size(ctypes.byref(p), b.ctypes.data_as(P)) == 0

@@ -134,3 +134,16 @@ def test_varlen_matches_separate_calls_bitwise(dev):
         assert torch.equal(one["vote"][0], res["vote"][b, :, :L - wl.l_obs])
         assert torch.equal(one["k_out"][0, :, :kb + wl.l_obs], res["k_out"][b, :, :kb + wl.l_obs])
         assert torch.equal(one["v_out"][0, :, :kb + wl.l_obs], res["v_out"][b, :, :kb + wl.l_obs])
+
+
+def test_varlen_with_a_sequence_that_keeps_nothing(dev):
+    """p * L_prefix < 1 for one short prompt: that sequence keeps only its window (k = 0), the others
+    keep their own k (the batch then takes one compression per sequence)."""
+    from kv_cache_compression_gb300 import snapkv
+    wl = synth.WORKLOADS[1].with_(heads=3, plants=16)
+    lengths = [3000, 50, 1500]
+    q, k, v = synth.device_inputs_padded(wl, 0, 0, lengths, dev)
+    res = snapkv.compress_varlen(q, k, v, lengths, pool_kernel=wl.pool_kernel, ratio_p=0.05, want_vote=True)
+    torch.cuda.synchronize()
+    assert res["ks"][1] == 0
+    _check(res, wl, lengths, range(wl.heads), ratio_p=0.05, budget=0)

@@ -181,8 +181,10 @@ SNAPKV_API snapkv_status snapkv_compress_gqa(const snapkv_compress_params* param
  * snapkv_compress_varlen — snapkv_compress of a batch whose prompts have different lengths: sequence
  * b has l_prompts[b] rows (host array, L_obs < l_prompts[b] <= params->l_prompt), so its prefix,
  * its window (the last L_obs of its own rows) and its k = floor(p * L_prefix_b) or
- * min(budget, L_prefix_b) ([SnapKV] 投票メカニズム) are its own. Each sequence is compressed as in
- * snapkv_compress, one after another on `stream`, into its slice of the shared outputs.
+ * min(budget, L_prefix_b) ([SnapKV] 投票メカニズム) are its own. Each sequence's result is what
+ * snapkv_compress of that sequence alone gives, written into its slice of the shared outputs. The
+ * tensor-core path takes the whole batch in one launch per kernel (up to 64 sequences, each keeping
+ * at least one row); otherwise the sequences are compressed one after another on `stream`.
  *
  * q_obs     device [B, H, L_obs, d]   each sequence's window queries
  * k, v      device [B, H, params->l_prompt, d], padded: sequence b's rows 0 .. l_prompts[b]-1 are read

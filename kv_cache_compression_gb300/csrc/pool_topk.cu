@@ -204,6 +204,7 @@ __device__ __forceinline__ uint32_t cta_exclusive_scan(uint32_t v, uint32_t* sh_
 // Shared-memory words of the cluster kernel: the pooled slice, then the vote with its halo during
 // the pool (this slice's histogram afterwards), then the two cluster-histogram buffers.
 constexpr int kHistWords = kMaxBins;
+constexpr int kPoolChunk = 4096;   // vote values (plus the pooling halo) staged at a time
 constexpr int kSumWords = 2 * kMaxBins;
 
 __host__ __device__ constexpr int round4(int x) { return (x + 3) & ~3; }
@@ -224,6 +225,7 @@ struct GatherArgs {
   int32_t* len_out;
   int64_t kv_stride, cap;   // rows between heads in k / v, rows per head in k_out / v_out
   int64_t c_stride, idx_stride;   // rows between heads in the vote and in the indices
+  int32_t* dev_status;            // consistency failures of the gather (a library bug) are reported here
   int vpr, l_obs, heads;
   // Ragged batch (n > 0): sequence s (= head / heads) has its own prefix length and kept count;
   // the kernel's l_prefix, k_sel and slice arguments are then the maxima.
@@ -234,15 +236,15 @@ struct GatherArgs {
   } var;
 };
 
-__global__ void __launch_bounds__(kCThreads)
+__global__ void __launch_bounds__(kCThreads, 2)   // two CTAs per SM (a 32-head layer in one wave)
 pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ idx_all, int64_t l_prefix,
                          int radius, int64_t k_sel, int slice, GatherArgs g) {
   extern __shared__ __align__(16) uint32_t sm[];
   uint32_t* pbits = sm;                                      // [slice] pooled vote bit patterns
   uint32_t* work = sm + round4(slice);                       // 16-B aligned
-  float* cbuf = reinterpret_cast<float*>(work);              // [slice + 2 * radius] vote with halo
+  float* cbuf = reinterpret_cast<float*>(work);              // [min(slice, kPoolChunk) + 2 * radius] vote + halo
   uint32_t* hist = work;                                     // [kMaxBins] this slice's histogram
-  uint32_t* sums = work + round4(max(slice + 2 * radius, kHistWords));   // [2][kMaxBins] cluster histograms
+  uint32_t* sums = work + round4(max(min(slice, kPoolChunk) + 2 * radius, kHistWords));   // [2][kMaxBins] cluster histograms
   // (the layout above is sized for the largest slice; a ragged batch's shorter sequences use less)
   uint32_t* sh_warp = sums + kSumWords;                      // [32]
   uint32_t* counts = sh_warp + 32;                           // [8 + 1] packed (greater << 16 | equal) per slice
@@ -266,20 +268,25 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   for (int b = tid; b < kSumWords; b += kCThreads) sums[b] = 0u;
   ptx::cluster_arrive();   // this CTA's cluster histograms are clear (waited for before the first add)
 
-  // Max pool of the slice: the vote (L2-resident) with its halo is staged in shared memory by
-  // coalesced independent loads, -inf outside the prefix; then each P_j is a max over the window.
-  const int h0 = j0 - radius, hn = n + 2 * radius;
-  for (int q = tid; q < hn; q += kCThreads) {
-    const int j = h0 + q;
-    cbuf[q] = (j >= 0 && j < L) ? __ldcg(c + j) : -INFINITY;
+  // Max pool of the slice, kPoolChunk values at a time: the vote (L2-resident) with its halo is
+  // staged in shared memory by coalesced independent loads, -inf outside the prefix; then each P_j
+  // is a max over the window. (The staging buffer stays small, so that a long prefix's slices leave
+  // room for two CTAs per SM.)
+  for (int ch0 = 0; ch0 < n; ch0 += kPoolChunk) {
+    const int cn = min(kPoolChunk, n - ch0);
+    const int h0 = j0 + ch0 - radius, hn = cn + 2 * radius;
+    for (int q = tid; q < hn; q += kCThreads) {
+      const int j = h0 + q;
+      cbuf[q] = (j >= 0 && j < L) ? __ldcg(c + j) : -INFINITY;
+    }
+    __syncthreads();
+    for (int j = tid; j < cn; j += kCThreads) {
+      float m = cbuf[j];
+      for (int q = 1; q <= 2 * radius; ++q) m = fmaxf(m, cbuf[j + q]);
+      pbits[ch0 + j] = __float_as_uint(m);
+    }
+    __syncthreads();   // the next chunk, and the histogram below, reuse the staging buffer
   }
-  __syncthreads();
-  for (int j = tid; j < n; j += kCThreads) {
-    float m = cbuf[j];
-    for (int q = 1; q <= 2 * radius; ++q) m = fmaxf(m, cbuf[j + q]);
-    pbits[j] = __float_as_uint(m);
-  }
-  __syncthreads();   // the histogram below reuses the staging buffer
   uint32_t prefix = 0, mask = 0, krem = (uint32_t)k_sel;
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0), nb = pass < 2 ? 2048 : 1024;   // 11 + 11 + 10 bits
@@ -366,6 +373,7 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   const uint32_t n_kept = (counts[kMaxCluster] >> 16) + (eq_end < need_eq ? eq_end : need_eq) -
                           (eq_before < need_eq ? eq_before : need_eq);
   uint32_t* kept = work;
+  const int kept_cap = round4(max(min(slice, kPoolChunk) + 2 * radius, kHistWords));   // the work space
   const uint32_t e0 = eq_before + (packed_in & 0xffffu);
   uint32_t pos = gt_before + (packed_in >> 16) + (e0 < need_eq ? e0 : need_eq);
   uint32_t e = e0;
@@ -379,7 +387,10 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
     if (keep) {
       if ((int64_t)pos < k_sel) {
         idx[pos] = j0 + j;
-        kept[pos - p0] = (uint32_t)(j0 + j);
+        if (pos - p0 < (uint32_t)kept_cap)
+          kept[pos - p0] = (uint32_t)(j0 + j);
+        else
+          report(g.dev_status, SNAPKV_ERR_INTERNAL);
       }
       ++pos;
     }
@@ -394,7 +405,14 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   uint4* kout = g.k_out + bh * g.cap * vpr;
   uint4* vout = g.v_out + bh * g.cap * vpr;
   const int n_win = (g.l_obs - (int)rank + (int)csize - 1) / (int)csize;   // window rows of this CTA
-  const int64_t items = ((int64_t)n_kept + n_win) * vpr;
+  // The kept rows land in [p0, p0 + n_kept) of the first k_sel cache rows, and every one of them
+  // was listed above; an inconsistent count would be a library bug: reported, not followed.
+  uint32_t n_rows = n_kept;
+  if ((int64_t)p0 + n_kept > k_sel || n_kept > (uint32_t)kept_cap) {
+    if (tid == 0) report(g.dev_status, SNAPKV_ERR_INTERNAL);
+    n_rows = 0;
+  }
+  const int64_t items = ((int64_t)n_rows + n_win) * vpr;
   constexpr int U = 4;
   for (int64_t base = tid; base < items; base += (int64_t)U * kCThreads) {
     uint4 kv[U], vv[U];
@@ -407,11 +425,11 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
         const int64_t row = it / vpr;
         const int c = (int)(it - row * vpr);
         int64_t src, out;
-        if (row < (int64_t)n_kept) {
+        if (row < (int64_t)n_rows) {
           src = kept[row];
           out = p0 + row;
         } else {
-          const int64_t t = (int64_t)rank + (row - n_kept) * csize;   // window row
+          const int64_t t = (int64_t)rank + (row - n_rows) * csize;   // window row
           src = l_prefix + t;
           out = k_sel + t;
         }
@@ -455,7 +473,7 @@ cudaError_t launch_pool_topk(const CompressJob& job, bool* gathered) {
     if (cl > kMaxCluster) cl = kMaxCluster;
     if (cl < 1) cl = 1;
     const int slice = (int)((job.l_prefix + cl - 1) / cl);
-    const int work = slice + 2 * (job.pool_kernel / 2);
+    const int work = (slice < kPoolChunk ? slice : kPoolChunk) + 2 * (job.pool_kernel / 2);
     const size_t smem =
         (size_t)(round4(slice) + round4(work > kHistWords ? work : kHistWords) + kSumWords + 32 + kMaxCluster + 1) *
         sizeof(uint32_t);
@@ -486,6 +504,7 @@ cudaError_t launch_pool_topk(const CompressJob& job, bool* gathered) {
     g.heads = job.heads;
     g.c_stride = job.l_prefix;
     g.idx_stride = job.k_sel;
+    g.dev_status = job.dev_status;
     g.var.n = 0;
     if (job.n_var > 0) {
       if (job.n_var > kMaxVarSeq) return cudaErrorInvalidValue;

@@ -500,6 +500,92 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       if (gtid == 0) ptx::red_add_release_u32(a.cnt + it.head, 1u);
     };
 
+    // A item for windows of 64 or more rows: two 32-row chunks share each exchange, so the item
+    // takes half the group barriers (the row maxima of pass 2 are read from shared memory).
+    auto item_stats_pairs = [&](int n, const Item& it) {
+      const int slot = n % kSlots;
+      const int tiles = tiles_of<VAR>(a, it, TI);
+      const int64_t item_key0 = (int64_t)it.chunk * a.keys_per_item;
+      const int64_t l_prompt = prompt_of<VAR>(a, it);
+      const int64_t l_prefix = VAR ? l_prompt - a.l_obs : a.l_prefix;
+      const int64_t lim = a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? l_prefix : l_prefix - 1;
+      // Folds the visible logits of rows rb .. rb + R - 1 of tile t into v (max or sum of 2^(s'-M)).
+      auto fold = [&](int t, int rb, float* v, bool sum) {
+        float acc[R];
+        load_rows((uint32_t)(slot * TI * N + t * N + rb), acc);
+        const int64_t tkey0 = item_key0 + t * kTileKeys;
+        if (tkey0 + kTileKeys <= l_prefix) {
+#pragma unroll
+          for (int i = 0; i < R; ++i)
+            v[i] = sum ? v[i] + ex2(fmaf(acc[i], a.scale_log2, -growc[rb + i])) : fmaxf(v[i], acc[i]);
+        } else {
+          const int64_t key = tkey0 + key_in_tile;
+#pragma unroll
+          for (int i = 0; i < R; ++i) {
+            const int row = rb + i;
+            const bool vis = row < a.l_obs && key < l_prompt &&
+                             (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + row : key <= lim);
+            if (vis) v[i] = sum ? v[i] + ex2(fmaf(acc[i], a.scale_log2, -growc[rb + i])) : fmaxf(v[i], acc[i]);
+          }
+        }
+      };
+      wait_tiles(slot, n / kSlots);
+#pragma unroll 1
+      for (int r0 = 0; r0 < N; r0 += 2 * R) {
+        {
+          float va[R], vb[R];
+#pragma unroll
+          for (int i = 0; i < R; ++i) va[i] = vb[i] = -INFINITY;
+          for (int t = 0; t < tiles; ++t) {
+            fold(t, r0, va, false);
+            fold(t, r0 + R, vb, false);
+          }
+          tc::butterfly_max<R, 16>(va, lane);
+          stash_rows(va, r0);
+          tc::butterfly_max<R, 16>(vb, lane);
+          stash_rows(vb, r0 + R);
+        }
+        ptx::named_barrier(bar_id, 128);
+        if (gtid < 2 * R) {
+          float mx = gred[r0 + gtid];
+#pragma unroll
+          for (int w = 1; w < 4; ++w) mx = fmaxf(mx, gred[w * N + r0 + gtid]);
+          growc[r0 + gtid] = mx * a.scale_log2;       // log2-domain row maximum (or -inf)
+        }
+        ptx::named_barrier(bar_id, 128);
+        const bool last_read = !a.resident && r0 + 2 * R >= N;   // resident items keep the slot
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const int rb = r0 + h * R;
+          float v[R];
+#pragma unroll
+          for (int i = 0; i < R; ++i) v[i] = 0.f;
+          for (int t = 0; t < tiles; ++t) fold(t, rb, v, true);
+          if (last_read && h == 1) ptx::tc_fence_before();
+          tc::butterfly_sum<R, 16>(v, lane);
+          stash_rows(v, rb);
+        }
+        ptx::named_barrier(bar_id, 128);
+        if (last_read && gtid == 0) ptx::mbar_arrive(&c.tmem_empty[slot]);
+        if (gtid < 2 * R && r0 + gtid < a.l_obs) {
+          float zz = gred[r0 + gtid];
+#pragma unroll
+          for (int w = 1; w < 4; ++w) zz += gred[w * N + r0 + gtid];
+          const float mx = growc[r0 + gtid];
+          if (zz > 0.f) {   // the row saw at least one visible key in this item
+            const float fl = floorf(mx);
+            if (fabsf(fl) > 1000.f) report(a.dev_status, SNAPKV_ERR_UNSUPPORTED);
+            const uint32_t fb = __float_as_uint(zz * ex2(mx - fl));
+            const long long e = (long long)fminf(fmaxf(fl, -1000.f), 1000.f) + (long long)((fb >> 23) & 0xFF) - 127;
+            const long long db = ((e + 1023) << 52) | ((long long)(fb & 0x7FFFFF) << 29);
+            ptx::red_add_f64(a.zsum + (int64_t)it.head * a.l_obs + r0 + gtid, __longlong_as_double(db));
+          }
+        }
+        ptx::named_barrier(bar_id, 128);
+      }
+      if (gtid == 0) ptx::red_add_release_u32(a.cnt + it.head, 1u);
+    };
+
     // B item (after its head's statistics are published): the vote of each prefix key,
     // C_j = sum_i 2^(s'_ij - c_i); the slot is released after the last TMEM read.
     auto item_vote = [&](int n, const Item& it) {
@@ -563,10 +649,14 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       const int p = blockIdx.x + n * gridDim.x;
       if (p >= a.n_queue || stop_uniform()) break;
       const Item it = queue_item<VAR>(a, p);
-      if (it.kind == 0)
-        item_stats(n, it);
-      else
+      if (it.kind == 0) {
+        if constexpr (N >= 2 * R)
+          item_stats_pairs(n, it);
+        else
+          item_stats(n, it);
+      } else {
         item_vote(n, it);
+      }
       if (a.resident && lag0) {
         // A head has at most one item on this CTA: its vote may wait for the head right away.
         item_vote(n, it);

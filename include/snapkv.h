@@ -101,6 +101,8 @@ typedef struct {
 
 /* Kept prefix slots per head, k (host-side, for sizing). Returns -1 if the params are invalid. */
 SNAPKV_API int64_t snapkv_compress_kept(const snapkv_compress_params* params);
+/* The same value under the name the sizing step is usually called by. */
+SNAPKV_API int64_t snapkv_compress_k(const snapkv_compress_params* params);
 
 /* Workspace bytes snapkv_compress needs for these params (0 if the params are invalid). */
 SNAPKV_API size_t snapkv_compress_workspace_size(const snapkv_compress_params* params);

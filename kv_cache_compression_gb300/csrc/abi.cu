@@ -122,6 +122,8 @@ int64_t snapkv_compress_kept(const snapkv_compress_params* params) {
   return k;
 }
 
+int64_t snapkv_compress_k(const snapkv_compress_params* params) { return snapkv_compress_kept(params); }
+
 size_t snapkv_compress_gqa_workspace_size(const snapkv_compress_params* params, int32_t q_heads) {
   int64_t lp = 0, k = 0;
   int rows = 0;

@@ -64,6 +64,8 @@ def lib():
         PP = ctypes.POINTER(CompressParams)
         L.snapkv_compress_kept.restype = I64
         L.snapkv_compress_kept.argtypes = [PP]
+        L.snapkv_compress_k.restype = I64
+        L.snapkv_compress_k.argtypes = [PP]
         L.snapkv_compress_workspace_size.restype = SZ
         L.snapkv_compress_workspace_size.argtypes = [PP]
         L.snapkv_compress.restype = I32
@@ -134,6 +136,10 @@ def make_params(*, batch, heads, head_dim, l_obs, l_prompt, pool_kernel, ratio_p
 
 def kept(params: CompressParams) -> int:
     return int(lib().snapkv_compress_kept(ctypes.byref(params)))
+
+
+def compress_k(params: CompressParams) -> int:
+    return int(lib().snapkv_compress_k(ctypes.byref(params)))
 
 
 def compress_workspace_size(params: CompressParams, q_heads=None) -> int:

@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = sk.declared_functions()
-    assert len(names) == 15
+    assert len(names) == 16
     for n in names:
         assert hasattr(lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", sk.library_path()], capture_output=True, text=True).stdout
@@ -49,6 +49,8 @@ def test_kept_slots_on_host(lib):
     assert sk.kept(_params(pool_kernel=4)) == -1          # even kernel unsupported
     assert sk.kept(_params(head_dim=96)) == -1
     assert sk.kept(_params(ratio_p=1.5)) == -1
+    for kw in ({}, {"budget": 7}, {"ratio_p": 1.0}, {"l_prompt": 32}):
+        assert sk.compress_k(_params(**kw)) == sk.kept(_params(**kw))   # the alias gives the same k
     assert sk.kept(_params(ratio_p=float("nan"))) == -1
 
 

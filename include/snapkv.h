@@ -118,7 +118,14 @@ SNAPKV_API size_t snapkv_compress_workspace_size(const snapkv_compress_params* p
  *   K_c  = [K[I]; K[L_prefix : L_prompt]],  V_c likewise   (length R = k + L_obs)
  *
  * q_obs     device [B, H, L_obs, d]     the window's queries (prompt rows L_prefix..L_prompt-1)
- * k, v      device [B, H, L_prompt, d]  the layer's prompt keys and values (not modified)
+ * k         device [B, H, L_prompt, d]  the layer's prompt keys (not modified)
+ * v         [B, H, L_prompt, d]         the layer's prompt values (not modified): device memory, or
+ *           page-locked host memory mapped into the device's address space (cudaHostAlloc, or
+ *           cudaHostRegister with mapping). Only the R kept and window rows of each head are read,
+ *           so values that live on the host cross the host link for those rows alone (method: the
+ *           non-selected prefix values are never needed). Pageable host memory is refused with
+ *           SNAPKV_ERR_INVALID_ARG; the type is looked up with cudaPointerGetAttributes, in
+ *           relaxed stream-capture mode so that the call may be captured into a CUDA graph.
  * k_out     device [B, H, cap, d]        rows 0..R-1 of every head are written; the rest untouched
  * v_out     device [B, H, cap, d]
  * cap       rows per head of k_out / v_out; must be >= R, else SNAPKV_ERR_CAPACITY
@@ -167,7 +174,8 @@ SNAPKV_API snapkv_status snapkv_compress_profiled(const snapkv_compress_params* 
  * KV head. G * L_obs <= 128 (else SNAPKV_ERR_UNSUPPORTED).
  *
  * q_obs     device [B, q_heads, L_obs, d]
- * k, v      device [B, heads, L_prompt, d]
+ * k         device [B, heads, L_prompt, d]
+ * v         [B, heads, L_prompt, d], device or mapped page-locked host memory as for snapkv_compress
  * vote_out  device fp32 [B, heads, L_prefix] (the summed vote; NULL: not returned)
  * every other argument as for snapkv_compress, with heads = KV heads; the workspace size is
  * snapkv_compress_gqa_workspace_size(params, q_heads).
@@ -189,7 +197,8 @@ SNAPKV_API snapkv_status snapkv_compress_gqa(const snapkv_compress_params* param
  * at least one row); otherwise the sequences are compressed one after another on `stream`.
  *
  * q_obs     device [B, H, L_obs, d]   each sequence's window queries
- * k, v      device [B, H, params->l_prompt, d], padded: sequence b's rows 0 .. l_prompts[b]-1 are read
+ * k, v      [B, H, params->l_prompt, d], padded: sequence b's rows 0 .. l_prompts[b]-1 are read;
+ *           k in device memory, v in device or mapped page-locked host memory (as for snapkv_compress)
  * k_out, v_out device [B, H, cap, d], cap >= k_max + L_obs where k_max = snapkv_compress_kept(params)
  *           (k grows with the prompt length); rows 0 .. k_b + L_obs - 1 of sequence b are written
  * len_out   device int32 [B], set to k_b + L_obs

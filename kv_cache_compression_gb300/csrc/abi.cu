@@ -26,6 +26,31 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
   return a0 < b0 + bn && b0 < a0 + an;
 }
 
+// V may be device memory or page-locked host memory mapped into the device's address space: the
+// compression reads only the kept rows and the window rows of V, so a caller whose values live on
+// the host need not copy the rest over the host link. Pageable host memory is refused. The query
+// runs in relaxed capture mode, so that a call being captured into a CUDA graph may make it.
+snapkv_status device_view_of_values(const void* v, const void** v_dev) {
+  cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+  if (cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  cudaPointerAttributes at{};
+  const cudaError_t e = cudaPointerGetAttributes(&at, v);
+  cudaThreadExchangeStreamCaptureMode(&mode);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return e == cudaErrorInvalidValue ? SNAPKV_ERR_INVALID_ARG : SNAPKV_ERR_CUDA;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+    *v_dev = v;
+    return SNAPKV_OK;
+  }
+  if (at.type == cudaMemoryTypeHost && at.devicePointer && aligned16(at.devicePointer)) {
+    *v_dev = at.devicePointer;
+    return SNAPKV_OK;
+  }
+  return SNAPKV_ERR_INVALID_ARG;
+}
+
 // Validates the problem statement (q_heads query heads share the params' KV heads); on success
 // fills l_prefix, k_sel and the window-query rows per KV head.
 snapkv_status check_params(const snapkv_compress_params* p, int32_t q_heads, int64_t* l_prefix, int64_t* k_sel,
@@ -195,6 +220,8 @@ snapkv_status compress_impl(const snapkv_compress_params* params, int32_t q_head
       overlaps(v, in_bytes, k_out, out_bytes) || overlaps(v, in_bytes, v_out, out_bytes) ||
       overlaps(k_out, out_bytes, v_out, out_bytes))
     return SNAPKV_ERR_INVALID_ARG;
+  const snapkv_status vs = device_view_of_values(v, &v);
+  if (vs != SNAPKV_OK) return vs;
 
   char* ws = static_cast<char*>(workspace);
   CompressJob job;
@@ -306,6 +333,8 @@ snapkv_status snapkv_compress_varlen(const snapkv_compress_params* params, const
       overlaps(v, in_bytes, k_out, out_bytes) || overlaps(v, in_bytes, v_out, out_bytes) ||
       overlaps(k_out, out_bytes, v_out, out_bytes))
     return SNAPKV_ERR_INVALID_ARG;
+  const snapkv_status vs = device_view_of_values(v, &v);
+  if (vs != SNAPKV_OK) return vs;
 
   const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);

@@ -164,7 +164,8 @@ def compress(q_obs, k, v, *, pool_kernel, ratio_p=0.0, budget=0, scope="prompt_c
     """snapkv_compress on torch tensors q_obs [B,Hq,L_obs,d], k, v [B,H,L_prompt,d].
 
     Hq > H (a multiple of H) is grouped-query attention (snapkv_compress_gqa): the Hq / H query
-    heads of each KV head vote together. Returns a dict with k_out, v_out ([B,H,cap,d]), len_out
+    heads of each KV head vote together. ``v`` may be a pinned CPU tensor: only its kept and window
+    rows are read, over the host link. Returns a dict with k_out, v_out ([B,H,cap,d]), len_out
     [B], idx [B,H,k] (if wanted) and vote [B,H,L_prefix] (if wanted), plus k (kept slots) and the
     workspace used.
     """
@@ -216,7 +217,8 @@ def compress_varlen(q_obs, k, v, l_prompts, *, pool_kernel, ratio_p=0.0, budget=
                     algo="auto", cap=None, want_idx=True, want_vote=False, workspace=None, dev_status=None,
                     stream=None, out=None):
     """snapkv_compress_varlen: q_obs [B,H,L_obs,d]; k, v [B,H,L_max,d] padded, sequence b using its
-    first l_prompts[b] rows. Returns k_out, v_out [B,H,cap,d], len [B], idx [B,H,k_max] (row b, h
+    first l_prompts[b] rows (``v`` may be a pinned CPU tensor, as for compress). Returns k_out, v_out
+    [B,H,cap,d], len [B], idx [B,H,k_max] (row b, h
     holds k_b indices), vote [B,H,L_max-L_obs] (if wanted), ks (per-sequence k) and the workspace.
     ``out``: a previous call's result whose buffers (outputs and workspace) this call writes again."""
     import numpy as np

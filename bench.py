@@ -562,6 +562,7 @@ def run_ours(args, rank, world, local_rank):
     k_out = torch.empty((B, H, cap, d), dtype=torch.bfloat16, device=dev)
     v_out = torch.empty_like(k_out)
     length = torch.zeros((B,), dtype=torch.int32, device=dev)
+    length_next = torch.zeros_like(length)   # the decode step's new lengths (its input stays `length`)
     idx = torch.empty((B, H, ksel), dtype=torch.int32, device=dev)
     out = torch.empty((B, H, d), dtype=torch.bfloat16, device=dev)
     status = torch.zeros((1,), dtype=torch.int32, device=dev)
@@ -573,8 +574,8 @@ def run_ours(args, rank, world, local_rank):
     n_ev = 2 * len(STAGES)
 
     def launch_step(i, strm, events=None):
-        """Enqueue one step on `strm`: compress (stage events recorded inside the library), append,
-        decode."""
+        """Enqueue one step on `strm`: compress (stage events recorded inside the library), then one
+        decode step (append + attention in one call)."""
         q, k, v = copies[i % N_COPIES]
         sh = ctypes.c_void_p(strm.cuda_stream)
         ev_arr = (ctypes.c_void_p * n_ev)(*[e.cuda_event for e in events[:n_ev]]) if events else None
@@ -584,10 +585,10 @@ def run_ours(args, rank, world, local_rank):
                                           P(status.data_ptr()), sh, ev_arr, n_ev if events else 0)
         if st != 0:
             raise RuntimeError(f"snapkv_compress: {snapkv.status_string(st)}")
-        snapkv.append(kn, vn, k_out, v_out, length, dev_status=status, stream=strm)
         if events:
             events[n_ev].record(strm)
-        snapkv.decode_attend(qn, k_out, v_out, length, out=out, workspace=ws_d, dev_status=status, stream=strm)
+        snapkv.append_decode_attend(qn, kn, vn, k_out, v_out, length, length_next, out=out, workspace=ws_d,
+                                    dev_status=status, stream=strm)
         if events:
             events[n_ev + 1].record(strm)
 
@@ -691,7 +692,7 @@ def run_ours(args, rank, world, local_rank):
     up_s, down_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     dev_in = [tuple(torch.empty_like(t, device=dev) for t in copies[0]) for _ in range(2)]
     dev_out = [(torch.empty_like(k_out), torch.empty_like(v_out), torch.empty_like(idx), torch.empty_like(out),
-                torch.zeros_like(length)) for _ in range(2)]
+                torch.zeros_like(length), torch.zeros_like(length)) for _ in range(2)]
     host_out = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in o[:4]) for o in dev_out]
     up_done = [torch.cuda.Event() for _ in range(2)]
     comp_done = [torch.cuda.Event() for _ in range(2)]
@@ -731,12 +732,12 @@ def run_ours(args, rank, world, local_rank):
             if i >= 2:
                 stream.wait_event(down_done[j])    # step i-2's outputs have reached the host
             dq, dk, dv = dev_in[j]
-            ko, vo, io, oo, ln = dev_out[j]
+            ko, vo, io, oo, ln, ln_next = dev_out[j]
             snapkv.compress(dq, dk, host_in[j][2] if v_on_host else dv, pool_kernel=wl.pool_kernel,
                             budget=wl.budget, cap=cap, k_out=ko, v_out=vo, len_out=ln, idx_out=io, workspace=ws_c,
                             dev_status=status, stream=stream)
-            snapkv.append(kn, vn, ko, vo, ln, dev_status=status, stream=stream)
-            snapkv.decode_attend(qn, ko, vo, ln, out=oo, workspace=ws_d, dev_status=status, stream=stream)
+            snapkv.append_decode_attend(qn, kn, vn, ko, vo, ln, ln_next, out=oo, workspace=ws_d, dev_status=status,
+                                        stream=stream)
             comp_done[j].record(stream)
             down_s.wait_event(comp_done[j])
             with torch.cuda.stream(down_s):
@@ -798,13 +799,13 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": units_per_step * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "path": "pinned host Q/K -> device; V stays in pinned host memory and snapkv.compress reads its "
-                        "kept and window rows over the host link (counted in h2d); append + decode_attend; "
+                        "kept and window rows over the host link (counted in h2d); append_decode_attend; "
                         "K_c/V_c/idx/out -> pinned host; two buffer sets, uploads and downloads on their own "
                         "streams overlap the neighbouring steps",
                 "upload_qk_alone_ms": upload_ms, "upload_gbs": (h2d - v_rows_bytes) / (upload_ms * 1e-3) / 1e9,
                 "v_uploaded": {"ms_per_step": e2e_all_ms, "value": units_per_step * world / (e2e_all_ms * 1e-3),
                                "h2d_bytes_per_step": h2d_all, "upload_qkv_alone_ms": upload_all_ms}},
-        "gpu_launches": args.steps * 4,   # vote, top-k (+ gather), append, decode
+        "gpu_launches": args.steps * 3,   # vote, top-k (+ gather), decode (+ append)
         "clocks": clocks,
         "wall_s_timed": wall,
         "kernel_source_sha256_16": src_hash,

@@ -255,6 +255,31 @@ SNAPKV_API snapkv_status snapkv_decode_attend(const void* q, const void* k_cache
                                    snapkv_stream_t stream);
 
 /*
+ * snapkv_append_decode_attend — one whole decode step ([KVcache] 22.2: append the new token's row,
+ * then attend over every cached row including it): the result of snapkv_append followed by
+ * snapkv_decode_attend, in one launch for caches of up to 16384 rows per head (the decode kernel
+ * writes the new row into the cache and into its own shared-memory copy of the rows before it
+ * attends). Longer caches take the two kernels one after the other.
+ *
+ * q, k_new, v_new   device [B, H, d]
+ * k_cache, v_cache  device [B, H, cap, d]; row len_in[b] of every head receives k_new / v_new
+ * len_in            device int32 [B], cached rows before this step (read only)
+ * len_out           device int32 [B], receives len_in[b] + 1 (len_in[b] when the row does not fit);
+ *                   must not overlap len_in, so a caller alternates two length arrays
+ * out               device [B, H, d], same dtype as the cache
+ * workspace         as for snapkv_decode_attend (snapkv_decode_workspace_size(B, H, d, cap))
+ * A sequence with len_in[b] >= cap (or < 0) is not appended, SNAPKV_ERR_CAPACITY is reported in
+ * *dev_status, and the attention covers its len_in[b] rows (clamped to cap) as snapkv_decode_attend
+ * would.
+ */
+SNAPKV_API snapkv_status snapkv_append_decode_attend(const void* q, const void* k_new, const void* v_new,
+                                                     void* k_cache, void* v_cache, int64_t cap,
+                                                     const int32_t* len_in, int32_t* len_out, void* out,
+                                                     int32_t batch, int32_t heads, int32_t head_dim,
+                                                     int32_t dtype, void* workspace, size_t workspace_bytes,
+                                                     int32_t* dev_status, snapkv_stream_t stream);
+
+/*
  * snapkv_decode_attend_noalloc — snapkv_decode_attend without a workspace argument, for callers
  * that cannot allocate device memory or hand one over: for example a plugin or custom-operator
  * interface that passes only inputs and outputs, or a latency-critical serving loop where a

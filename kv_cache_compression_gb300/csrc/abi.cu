@@ -524,6 +524,58 @@ snapkv_status snapkv_decode_attend(const void* q, const void* k_cache, const voi
   return SNAPKV_OK;
 }
 
+snapkv_status snapkv_append_decode_attend(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                          void* v_cache, int64_t cap, const int32_t* len_in, int32_t* len_out,
+                                          void* out, int32_t batch, int32_t heads, int32_t head_dim, int32_t dtype,
+                                          void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                          snapkv_stream_t stream) {
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !len_in || !len_out || !out) return SNAPKV_ERR_INVALID_ARG;
+  if (batch < 1 || heads < 1 || head_dim < 1 || cap < 1 || cap > kMaxPrompt) return SNAPKV_ERR_INVALID_ARG;
+  if (dtype != SNAPKV_F32 && dtype != SNAPKV_BF16) return SNAPKV_ERR_INVALID_ARG;
+  if ((int64_t)batch * heads > 65535) return SNAPKV_ERR_INVALID_ARG;  // grid.y limit
+  if (head_dim != 64 && head_dim != 128) return SNAPKV_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(out) || ((uintptr_t)len_in & 3u) || ((uintptr_t)len_out & 3u) || ((uintptr_t)dev_status & 3u))
+    return SNAPKV_ERR_INVALID_ARG;
+  // Every head reads len_in[b] while the new lengths are written: the two arrays must not overlap.
+  if (overlaps(len_in, (size_t)batch * 4, len_out, (size_t)batch * 4)) return SNAPKV_ERR_INVALID_ARG;
+  const DecodeLayout L = decode_layout(batch, heads, head_dim, cap);
+  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SNAPKV_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+  DecodeJob job;
+  job.batch = batch;
+  job.heads = heads;
+  job.head_dim = head_dim;
+  job.dtype = dtype;
+  job.cap = cap;
+  job.q = q;
+  job.k_cache = k_cache;
+  job.v_cache = v_cache;
+  job.len = len_in;
+  job.out = out;
+  job.partial = reinterpret_cast<float*>(ws + L.partial);
+  job.tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
+  job.split_rows = L.split_rows;
+  job.n_split = L.n_split;
+  job.dev_status = dev_status;
+  job.stream = strm;
+  if (cap <= decode_fuses_append_max_cap()) {   // one launch: the decode kernel appends first
+    job.k_new = k_new;
+    job.v_new = v_new;
+    job.len_out = len_out;
+  } else {   // longer caches: the new lengths start as a copy, the append kernel then updates them
+    if (cudaMemcpyAsync(len_out, len_in, (size_t)batch * 4, cudaMemcpyDeviceToDevice, strm) != cudaSuccess)
+      return SNAPKV_ERR_CUDA;
+    if (launch_append(k_new, v_new, k_cache, v_cache, cap, len_out, batch, heads, head_dim, dtype, dev_status,
+                      strm) != cudaSuccess)
+      return SNAPKV_ERR_CUDA;
+    job.len = len_out;
+  }
+  if (launch_decode(job) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  return SNAPKV_OK;
+}
+
 snapkv_status snapkv_decode_attend_noalloc(const void* q, const void* k_cache, const void* v_cache, int64_t cap,
                                            const int32_t* len, void* out, int32_t batch, int32_t heads,
                                            int32_t head_dim, int32_t dtype, int32_t* dev_status,

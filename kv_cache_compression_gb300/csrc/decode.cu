@@ -88,6 +88,9 @@ struct DecArgs {
   int heads, split_rows, n_split;
   float scale_log2;
   int32_t* dev_status;
+  const void* k_new;   // fused append (cluster kernel): the new token's K and V rows [B, H, d], or null
+  const void* v_new;
+  int32_t* len_out;    // fused append: the new lengths [B]
 };
 
 template <typename T> __device__ __forceinline__ void store_out(T* p, float x);
@@ -271,6 +274,12 @@ constexpr int kClChunkBytes = 16 * 1024;
 constexpr int kClBufs = 3;
 constexpr long long kClWaitLimit = 4000000000LL;   // ~2 s of SM clock
 
+// Orders this thread's generic-proxy writes to shared memory before later async-proxy (bulk copy)
+// accesses of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(DecArgs a) {
   constexpr int V = Elem<T>::kVec;
@@ -318,6 +327,20 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(DecArgs a) {
     for (int c = 0; c < nchunks && c < kClBufs; ++c) issue(c);
 
   int n = a.len[b];
+  // Fused append ([KVcache] 22.2: the cache grows by the new token's row, then attention covers
+  // it): the row goes to cache row n when n < cap, the attention then covers n + 1 rows, and the
+  // first head's cluster records the new length; a full cache is reported and left unchanged.
+  int new_row = -1;
+  if (a.k_new) {
+    const bool first = rank == 0 && tid == 0 && bh % a.heads == 0;
+    if (n >= 0 && n < cap) {
+      new_row = n;
+      n += 1;
+    } else if (first) {
+      report(a.dev_status, SNAPKV_ERR_CAPACITY);
+    }
+    if (first) a.len_out[b] = n;
+  }
   if ((int64_t)n > a.cap) {
     if (rank == 0 && tid == 0 && bh % a.heads == 0) report(a.dev_status, SNAPKV_ERR_CAPACITY);
     n = cap;
@@ -325,6 +348,17 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(DecArgs a) {
   if (n < 0) n = 0;
   const int sub = lane / LPR, cl = lane % LPR;
   const int group = warp * RPW + sub;
+  // The CTA whose rows hold the new row writes it into the chunk's shared-memory copy (after that
+  // chunk lands, before any group reads it) and into the cache; its first 2 * PIECES threads hold
+  // the row's 16-byte pieces (K, then V) from the start.
+  constexpr int PIECES = ROW_BYTES / 16;
+  const bool owns_new = new_row >= r0 && new_row < r1;
+  const int new_chunk = owns_new ? (new_row - r0) / CH : -1;
+  uint4 new_piece = make_uint4(0u, 0u, 0u, 0u);
+  if (owns_new && tid < 2 * PIECES) {
+    const uint4* src = static_cast<const uint4*>(tid < PIECES ? a.k_new : a.v_new) + bh * PIECES;
+    new_piece = ld_nc_v4(src + tid % PIECES);
+  }
 
   const T* qp = static_cast<const T*>(a.q) + bh * D;
   float q[V];
@@ -339,6 +373,18 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(DecArgs a) {
   for (int c = 0; c < nchunks; ++c) {
     const int buf = c % kClBufs;
     if (!ptx::mbar_wait(&bar[buf], (uint32_t)((c / kClBufs) & 1), &no_abort, kClWaitLimit)) timed_out = true;
+    if (c == new_chunk) {   // uniform in the CTA
+      if (tid < 2 * PIECES) {
+        const int rr = new_row - (r0 + c * CH);
+        uint8_t* srow = dsm + (2 * buf + (tid < PIECES ? 0 : 1)) * kClChunkBytes + rr * ROW_BYTES;
+        *reinterpret_cast<uint4*>(srow + (tid % PIECES) * 16) = new_piece;
+        // The caches of the fused entry point are writable; the chunk's copy of this row has landed.
+        T* crow = const_cast<T*>(tid < PIECES ? kc : vc) + (int64_t)new_row * D;
+        reinterpret_cast<uint4*>(crow)[tid % PIECES] = new_piece;
+        fence_proxy_async_smem();   // before a later bulk copy refills this buffer
+      }
+      __syncthreads();
+    }
     const uint8_t* kbuf = dsm + (2 * buf) * kClChunkBytes;
     const uint8_t* vbuf = kbuf + kClChunkBytes;
     const int cr0 = r0 + c * CH;
@@ -477,6 +523,8 @@ cudaError_t launch_decode_typed(const DecodeJob& job, const DecArgs& a) {
 
 }  // namespace
 
+int64_t decode_fuses_append_max_cap() { return kClusterMaxCap; }
+
 DecodeLayout decode_layout(int batch, int heads, int head_dim, int64_t cap) {
   DecodeLayout L;
   // 128-row splits, or longer ones (a multiple of 128) for caches beyond 512 splits: the merge
@@ -558,6 +606,10 @@ cudaError_t launch_decode(const DecodeJob& job) {
   a.n_split = job.n_split;
   a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)job.head_dim));
   a.dev_status = job.dev_status;
+  a.k_new = job.k_new;
+  a.v_new = job.v_new;
+  a.len_out = job.len_out;
+  if (job.k_new && job.cap > kClusterMaxCap) return cudaErrorInvalidValue;   // the ABI appends separately
   if (job.cap <= kClusterMaxCap) {
     if (job.dtype == SNAPKV_BF16)
       return job.head_dim == 64 ? launch_decode_cluster<__nv_bfloat16, 64>(job, a)

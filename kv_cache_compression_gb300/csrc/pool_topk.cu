@@ -398,7 +398,8 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   __syncthreads();
 
   // Gather: this CTA's kept rows, then window rows rank, rank + csize, ... (16-byte pieces, four
-  // rows' worth of loads in flight per thread).
+  // rows' worth of loads in flight per thread; the destinations are recomputed for the stores
+  // rather than held in registers across the loads, which keeps the kernel free of spills).
   const int vpr = g.vpr;
   const uint4* kin = g.k + bh * g.kv_stride * vpr;
   const uint4* vin = g.v + bh * g.kv_stride * vpr;
@@ -414,35 +415,30 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   }
   const int64_t items = ((int64_t)n_rows + n_win) * vpr;
   constexpr int U = 4;
+  const int vsh = __ffs(vpr) - 1;   // 16-byte pieces per row: 8, 16 or 32
   for (int64_t base = tid; base < items; base += (int64_t)U * kCThreads) {
     uint4 kv[U], vv[U];
-    int64_t dst[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t it = base + (int64_t)u * kCThreads;
-      dst[u] = -1;
       if (it < items) {
-        const int64_t row = it / vpr;
-        const int c = (int)(it - row * vpr);
-        int64_t src, out;
-        if (row < (int64_t)n_rows) {
-          src = kept[row];
-          out = p0 + row;
-        } else {
-          const int64_t t = (int64_t)rank + (row - n_rows) * csize;   // window row
-          src = l_prefix + t;
-          out = k_sel + t;
-        }
-        dst[u] = out * vpr + c;
+        const int64_t row = it >> vsh;
+        const int c = (int)(it & (vpr - 1));
+        const int64_t src = row < (int64_t)n_rows ? (int64_t)kept[row]
+                                                  : l_prefix + (int64_t)rank + (row - n_rows) * csize;
         kv[u] = ld_stream_v4(kin + src * vpr + c);
         vv[u] = ld_stream_v4(vin + src * vpr + c);
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (dst[u] >= 0) {
-        kout[dst[u]] = kv[u];
-        vout[dst[u]] = vv[u];
+      const int64_t it = base + (int64_t)u * kCThreads;
+      if (it < items) {
+        const int64_t row = it >> vsh;
+        const int c = (int)(it & (vpr - 1));
+        const int64_t out = row < (int64_t)n_rows ? (int64_t)p0 + row : k_sel + (int64_t)rank + (row - n_rows) * csize;
+        kout[out * vpr + c] = kv[u];
+        vout[out * vpr + c] = vv[u];
       }
     }
   }

@@ -96,7 +96,16 @@ struct DecodeJob {
   int split_rows, n_split;
   int32_t* dev_status;
   cudaStream_t stream;
+  // Fused append (k_new non-null; caches of at most decode_fuses_append_max_cap() rows): row
+  // len[b] of every head of sequence b takes the new token's K and V (when it fits) before the
+  // attention, which then covers len[b] + 1 rows, and len_out[b] receives the new length.
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  int32_t* len_out = nullptr;
 };
+
+// Largest cache (rows per head) whose decode kernel can take the append along.
+int64_t decode_fuses_append_max_cap();
 
 struct DecodeLayout {
   size_t partial, tickets, total;

@@ -78,6 +78,8 @@ def lib():
         L.snapkv_decode_workspace_size.argtypes = [I32, I32, I32, I64]
         L.snapkv_decode_attend.restype = I32
         L.snapkv_decode_attend.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, P, SZ, P, P]
+        L.snapkv_append_decode_attend.restype = I32
+        L.snapkv_append_decode_attend.argtypes = [P, P, P, P, P, I64, P, P, P, I32, I32, I32, I32, P, SZ, P, P]
         L.snapkv_decode_attend_noalloc.restype = I32
         L.snapkv_decode_attend_noalloc.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, P, P]
         L.snapkv_compress_gqa_workspace_size.restype = SZ
@@ -309,3 +311,25 @@ def decode_attend(q, k_cache, v_cache, len_, *, out=None, workspace=None, dev_st
     if st != OK:
         raise SnapKVError(st, "snapkv_decode_attend")
     return out
+
+
+def append_decode_attend(q, k_new, v_new, k_cache, v_cache, len_in, len_out=None, *, out=None, workspace=None,
+                         dev_status=None, stream=None):
+    """snapkv_append_decode_attend: append k_new, v_new [B,H,d] at row len_in[b], then attend with q [B,H,d]
+    over the len_in[b] + 1 rows. Returns (out [B,H,d], len_out [B]); len_out must not be len_in."""
+    import torch
+    B, H, cap, d = k_cache.shape
+    if out is None:
+        out = torch.empty((B, H, d), dtype=k_cache.dtype, device=k_cache.device)
+    if len_out is None:
+        len_out = torch.empty_like(len_in)
+    if workspace is None:
+        workspace = new_workspace(decode_workspace_size(B, H, d, cap), k_cache.device)
+    st = lib().snapkv_append_decode_attend(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                           int(cap), _ptr(len_in), _ptr(len_out), _ptr(out), B, H, d,
+                                           _dtype_code(k_cache), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                                           _stream_handle(stream))
+    if st != OK:
+        raise SnapKVError(st, "snapkv_append_decode_attend")
+    return out, len_out

@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = sk.declared_functions()
-    assert len(names) == 16
+    assert len(names) == 17
     for n in names:
         assert hasattr(lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", sk.library_path()], capture_output=True, text=True).stdout
@@ -101,6 +101,19 @@ def test_decode_and_append_reject_bad_arguments(lib):
         == sk.ERR_WORKSPACE
     assert lib.snapkv_decode_attend(P(16), P(32), P(48), 10, P(64), P(88), 1, 1, 64, 0, P(256), 1 << 20, None,
                                     None) == sk.ERR_INVALID_ARG               # misaligned output
+    f = lib.snapkv_append_decode_attend
+    ok = dict(q=P(16), kn=P(32), vn=P(48), kc=P(64), vc=P(80), lin=P(96), lout=P(112), out=P(128))
+
+    def fused(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["kn"], a["vn"], a["kc"], a["vc"], 10, a["lin"], a["lout"], a["out"], 2, 1, 64, 0,
+                 a.get("ws", P(256)), 1 << 20, None, None)
+    assert fused(kn=None) == sk.ERR_INVALID_ARG
+    assert fused(lout=None) == sk.ERR_INVALID_ARG
+    assert fused(lout=P(100)) == sk.ERR_INVALID_ARG          # overlaps len_in (two sequences, 8 bytes)
+    assert fused(lout=P(96)) == sk.ERR_INVALID_ARG           # the same array
+    assert fused(vn=P(40)) == sk.ERR_INVALID_ARG             # misaligned new row
+    assert fused(ws=None) == sk.ERR_WORKSPACE
 
 
 def test_gqa_rejects_bad_groupings(lib):

@@ -55,6 +55,46 @@ def test_decode_zero_length_gives_zero_and_overlong_is_reported(dev):
     assert torch.equal(out[1], full[1])     # clamped to the capacity
 
 
+@pytest.mark.parametrize("dtype,d,cap", [(torch.bfloat16, 128, 700), (torch.bfloat16, 64, 700),
+                                         (torch.float32, 128, 700), (torch.float32, 64, 129),
+                                         (torch.bfloat16, 128, 20000)])
+def test_fused_append_decode_equals_the_two_calls(dev, dtype, d, cap):
+    """snapkv_append_decode_attend leaves the bytes snapkv_append then snapkv_decode_attend leave
+    (cache, new lengths, output), for sequences appending at row 0, row 1, mid-cache and the last
+    free row, and a full one (reported, not appended); caches beyond 16384 rows take the two
+    kernels in turn."""
+    from kv_cache_compression_gb300 import snapkv
+    g = torch.Generator().manual_seed(cap + d)
+    B, H = 5, 3
+    lens = [0, 1, cap // 2, cap - 1, cap]
+    kc = torch.randn(B, H, cap, d, generator=g).to(dtype).to(dev)
+    vc = torch.randn(B, H, cap, d, generator=g).to(dtype).to(dev)
+    q = (torch.randn(B, H, d, generator=g) * 2).to(dtype).to(dev)
+    kn = torch.randn(B, H, d, generator=g).to(dtype).to(dev)
+    vn = torch.randn(B, H, d, generator=g).to(dtype).to(dev)
+    length = torch.tensor(lens, dtype=torch.int32, device=dev)
+    kc1, vc1, len1 = kc.clone(), vc.clone(), length.clone()
+    st1 = torch.zeros(1, dtype=torch.int32, device=dev)
+    snapkv.append(kn, vn, kc1, vc1, len1, dev_status=st1)
+    out1 = snapkv.decode_attend(q, kc1, vc1, len1, dev_status=st1)
+    kc2, vc2 = kc.clone(), vc.clone()
+    st2 = torch.zeros(1, dtype=torch.int32, device=dev)
+    out2, len2 = snapkv.append_decode_attend(q, kn, vn, kc2, vc2, length, dev_status=st2)
+    torch.cuda.synchronize()
+    assert length.cpu().tolist() == lens                   # len_in is only read
+    assert len2.cpu().tolist() == len1.cpu().tolist() == [1, 2, cap // 2 + 1, cap, cap]
+    assert int(st1.item()) == int(st2.item()) == snapkv.ERR_CAPACITY
+    assert torch.equal(kc2, kc1) and torch.equal(vc2, vc1)
+    assert torch.equal(out2, out1)
+    o = to_numpy_f32(out2)
+    for b in (0, 3):
+        n = lens[b]
+        kref = torch.cat([kc[b, 1, :n], kn[b, 1][None]]).float().cpu().numpy()
+        vref = torch.cat([vc[b, 1, :n], vn[b, 1][None]]).float().cpu().numpy()
+        check_decode(o[b, 1], orc.decode_attend(q[b, 1].float().cpu().numpy(), kref, vref), dtype == torch.bfloat16,
+                     where=f"fused b{b} n{n}")
+
+
 def test_append_writes_row_and_advances_length(dev):
     from kv_cache_compression_gb300 import snapkv
     B, H, cap, d = 3, 4, 10, 64
@@ -98,10 +138,12 @@ def test_uncompressed_cache_decode_equals_full_causal_attention(dev):
             check_decode(to_numpy_f32(outs[t][0, h]), orc.decode_attend(qn, kc, vc), True, where=f"h{h} t{t}")
 
 
-def test_compressed_decode_workload_sampled(dev):
+@pytest.mark.parametrize("fused", [False, True], ids=["append+decode", "fused"])
+def test_compressed_decode_workload_sampled(dev, fused):
     """The ragged-prompt decode workload on sampled (sequence, layer): compress into a cache of
-    capacity 2048 + L_obs + 128, then all 128 decode steps of append + attention, checked against
-    the oracle re-simulating compression and every step on sampled heads."""
+    capacity 2048 + L_obs + 128, then all 128 decode steps of append + attention (two calls, or the
+    fused call with two length arrays in turn), checked against the oracle re-simulating
+    compression and every step on sampled heads."""
     from kv_cache_compression_gb300 import snapkv
     wl = synth.WORKLOADS[4]
     lens = wl.prompt_lengths()
@@ -113,12 +155,18 @@ def test_compressed_decode_workload_sampled(dev):
         del q, k, v
         ws = snapkv.new_workspace(snapkv.decode_workspace_size(1, wl.heads, wl.head_dim, cap), dev)
         outs = []
+        len_bufs = [res["len"], torch.empty_like(res["len"])]
         for t in range(wl.decode_steps):
             qn, kn, vn = synth.device_decode_tokens(wl, layer, t, seq, 1, dev)
-            snapkv.append(kn, vn, res["k_out"], res["v_out"], res["len"])
-            outs.append(snapkv.decode_attend(qn, res["k_out"], res["v_out"], res["len"], workspace=ws)[0, heads].cpu())
+            if fused:
+                o, _ = snapkv.append_decode_attend(qn, kn, vn, res["k_out"], res["v_out"], len_bufs[t % 2],
+                                                   len_bufs[(t + 1) % 2], workspace=ws)
+            else:
+                snapkv.append(kn, vn, res["k_out"], res["v_out"], res["len"])
+                o = snapkv.decode_attend(qn, res["k_out"], res["v_out"], res["len"], workspace=ws)
+            outs.append(o[0, heads].cpu())
         torch.cuda.synchronize()
-        assert res["len"].item() == cap
+        assert len_bufs[wl.decode_steps % 2 if fused else 0].item() == cap
         for j, h in enumerate(heads):
             hi = synth.host_head(wl, layer, seq, h, l_prompt=L)
             ref = orc.compress_head(hi.q_obs, hi.k, hi.v, pool_kernel=wl.pool_kernel, budget=wl.budget)

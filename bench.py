@@ -752,7 +752,7 @@ def run_ours(args, rank, world, local_rank):
 
     upload_ms = upload_alone(2)
     upload_all_ms = upload_alone(3)
-    e2e_all_ms = pipelined(False)
+    e2e_all_ms = min(pipelined(False), pipelined(False))   # context only: the better of two runs
     e2e_ms = pipelined(True)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status after the end-to-end steps: {snapkv.status_string(int(status.item()))}")

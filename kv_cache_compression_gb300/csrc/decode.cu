@@ -11,6 +11,9 @@
 //     shared memory. No workspace is touched.
 //   * longer caches: splits of `split_rows` rows, one CTA each, partials in the workspace, and the
 //     last CTA of the head to finish (an atomic ticket, no waiting) merges them.
+// The cluster kernel can also take the step's append along (snapkv_append_decode_attend): the
+// CTA whose rows hold the new row writes it into the cache and into its shared-memory copy before
+// the attention reads it. The separate append kernel serves snapkv_append and longer caches.
 #include <mutex>
 
 #include "sm100_ptx.cuh"

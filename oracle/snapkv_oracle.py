@@ -22,7 +22,7 @@ Sources (page title, section / equation):
              V_cache, every cached position visible), 22.4 (M_KV = 2 B S L H_KV d_h b),
              22.7 (cached decode equals full causal attention, float64, atol = rtol = 1e-10).
 
-Readings where the pages are open (each is listed in the design doc):
+Readings where the pages are open:
   * Softmax scope: rows are normalised over every prompt column the window query can see (all
     prefix columns plus the window columns up to and including its own position); the vote keeps
     the prefix columns. The restated listing normalises over the prefix columns only; that

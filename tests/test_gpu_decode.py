@@ -95,6 +95,31 @@ def test_fused_append_decode_equals_the_two_calls(dev, dtype, d, cap):
                      where=f"fused b{b} n{n}")
 
 
+def test_bench_step_launch_configuration(dev):
+    """The benchmark's step as it is timed: the Llama-2-7B-shaped layer compressed into a cache of
+    capacity k + L_obs + 1, then one fused decode step filling its last row; every head's output
+    against the oracle's decode over that head's cache rows (compression parity is checked on
+    every head elsewhere), and the new length."""
+    from kv_cache_compression_gb300 import snapkv
+    wl = synth.WORKLOADS[1]
+    q, k, v, _ = synth.device_inputs(wl, 0, 0, 1, wl.l_prompt, dev)
+    cap = wl.budget + wl.l_obs + 1
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, budget=wl.budget, cap=cap, dev_status=status)
+    qn, kn, vn = synth.device_decode_tokens(wl, 0, 0, 0, 1, dev)
+    out, len_next = snapkv.append_decode_attend(qn, kn, vn, res["k_out"], res["v_out"], res["len"],
+                                                dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert res["len"].item() == cap - 1 and len_next.item() == cap
+    o = to_numpy_f32(out)
+    kc, vc = to_numpy_f32(res["k_out"]), to_numpy_f32(res["v_out"])
+    for h in range(wl.heads):
+        qh, kh, vh = synth.host_decode_token(wl, 0, 0, h, 0)
+        assert np.array_equal(kc[0, h, cap - 1], kh) and np.array_equal(vc[0, h, cap - 1], vh)
+        check_decode(o[0, h], orc.decode_attend(qh, kc[0, h], vc[0, h]), True, where=f"head {h}")
+
+
 def test_append_writes_row_and_advances_length(dev):
     from kv_cache_compression_gb300 import snapkv
     B, H, cap, d = 3, 4, 10, 64

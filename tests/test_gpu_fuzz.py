@@ -38,7 +38,7 @@ def _compress_cases(n, seed):
     return cases
 
 
-@pytest.mark.parametrize("case", _compress_cases(16, 20261202), ids=lambda c: f"fuzz{c[0]}")
+@pytest.mark.parametrize("case", _compress_cases(32, 20261202), ids=lambda c: f"fuzz{c[0]}")
 def test_fuzz_compress(dev, case):
     from kv_cache_compression_gb300 import snapkv
     i, bf16, d, l_obs, L, pool, p, budget, scope, B, H = case
@@ -66,7 +66,7 @@ def test_fuzz_compress(dev, case):
                                     l_prefix=l_prefix, l_obs=l_obs, where=f"fuzz {i} {algo} b{b} h{h}")
 
 
-@pytest.mark.parametrize("seed", [1, 2, 3])
+@pytest.mark.parametrize("seed", [1, 2, 3, 8, 9])
 def test_fuzz_varlen(dev, seed):
     from kv_cache_compression_gb300 import snapkv
     rng = np.random.default_rng(1000 + seed)
@@ -90,7 +90,7 @@ def test_fuzz_varlen(dev, seed):
                                 k_in=hi.k, v_in=hi.v, l_prefix=lp, l_obs=l_obs, where=f"varlen seed {seed} b{b} h{h}")
 
 
-@pytest.mark.parametrize("seed", [4, 5, 6, 7])
+@pytest.mark.parametrize("seed", [4, 5, 6, 7, 10, 11])
 def test_fuzz_decode(dev, seed):
     from kv_cache_compression_gb300 import snapkv
     rng = np.random.default_rng(2000 + seed)
@@ -114,3 +114,14 @@ def test_fuzz_decode(dev, seed):
                 continue
             ref = orc.decode_attend(q[b, h].float().numpy(), kc[b, h, :n].float().numpy(), vc[b, h, :n].float().numpy())
             check_decode(o[b, h], ref, dtype == torch.bfloat16, where=f"seed {seed} b{b} h{h} n{n} cap {cap}")
+    # one decode step as the fused call and as append + decode: the same bytes
+    kn = torch.randn(B, H, d, generator=g).to(dtype).to(dev)
+    vn = torch.randn(B, H, d, generator=g).to(dtype).to(dev)
+    qd, length = q.to(dev), torch.tensor(lens, dtype=torch.int32).to(dev)
+    k1, v1, len1 = kc.to(dev), vc.to(dev), length.clone()
+    snapkv.append(kn, vn, k1, v1, len1)
+    out1 = snapkv.decode_attend(qd, k1, v1, len1)
+    k2, v2 = kc.to(dev), vc.to(dev)
+    out2, len2 = snapkv.append_decode_attend(qd, kn, vn, k2, v2, length)
+    torch.cuda.synchronize()
+    assert torch.equal(len2, len1) and torch.equal(k2, k1) and torch.equal(v2, v1) and torch.equal(out2, out1)

@@ -30,7 +30,9 @@
 //               buffers;
 //   warp 1      MMA: one thread issues tcgen05.mma (M = 128 keys, N = padded L_obs, K = 16) for each
 //               tile into the item's TMEM slot (four slots of 128 columns);
-//   warps 2..9  epilogue: two warpgroups, one thread per key (TMEM lane); warpgroup g takes the
+//   warps 2, 3  idle: with warps 0 and 1 they form warpgroup 0, which lowers its registers
+//               (setmaxnreg) so that the epilogue warpgroups can raise theirs;
+//   warps 4..11 epilogue: two warpgroups, one thread per key (TMEM lane); warpgroup g takes the
 //               CTA's items n = g, g + 2, ..., reads their logits with tcgen05.ld and gives the slot
 //               back as soon as it has read it.
 //
@@ -51,9 +53,20 @@
 namespace snapkv {
 namespace {
 
-constexpr int kEpiWarps = 8;                       // two warpgroups of epilogue warps
+constexpr int kCtlWarps = 4;                       // warpgroup 0: TMA producer, MMA issuer, two idle
+constexpr int kEpiWarps = 8;                       // warpgroups 1 and 2: the epilogue
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreadsTc = 64 + kEpiThreads;
+constexpr int kThreadsTc = kCtlWarps * 32 + kEpiThreads;
+// Register split (setmaxnreg): 12 warps put three warps on every SM sub-partition, so the launch
+// gives each thread 168 registers; warpgroup 0 then hands most of its share to the epilogue
+// warpgroups, which hold a 32-row chunk of logits per thread without spilling. The split uses
+// exactly the launch's registers (a larger request would wait for ever), and the host launches
+// the kernel only if the compiler gave it that count.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtlRegs = 56;
+constexpr int kEpiRegs = 224;
+static_assert(kCtlWarps * 32 * kCtlRegs + kEpiThreads * kEpiRegs == kThreadsTc * kLaunchRegs, "register split");
+constexpr int kTeardownBarrier = 3;                // named barrier of all warps before TMEM is freed
 constexpr int kTileKeys = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clock
@@ -251,6 +264,20 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
   __shared__ int no_abort;
   if (threadIdx.x == 0) no_abort = 0;
   __syncthreads();
+  // Every role ends here and returns: the roles' code paths never join again, so each compiles
+  // within its own register share.
+  auto teardown = [&]() {
+    __syncwarp();   // the roles' single-lane loops have rejoined their warps
+    ptx::named_barrier(kTeardownBarrier, kThreadsTc);   // every warp is done with TMEM
+    if (warp == 1) {
+      ptx::tc_fence_after();
+      ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+  };
+  if (warp < kCtlWarps)   // warpgroup-uniform
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
+  else
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -309,6 +336,8 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       for (int k = (n > 2 ? n - 2 : 0); k < n; ++k)
         ptx::mbar_wait(&c.q_full[k & 1], (k >> 1) & 1, &no_abort, kDrainLimit);
     }
+    teardown();
+    return;
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -359,12 +388,17 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       ptx::mma_commit(c.final_bar);
       ptx::mbar_wait(c.final_bar, 0, &no_abort, kDrainLimit);
     }
+    teardown();
+    return;
+  } else if (warp < kCtlWarps) {
+    teardown();   // warps 2 and 3 only lend their registers
+    return;
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..9)
+    // ------------------------------------------------------------ epilogue (warps 4..11)
     const int q4 = warp & 3;                         // TMEM lane quarter this warp may access
-    const int gw = (warp - 2) & 3;                   // warp within its group
-    const int grp = (warp - 2) >> 2;                 // group: items n = grp, grp + 2, ...
-    const int gtid = (threadIdx.x - 64) & 127;       // thread within its group
+    const int gw = (warp - kCtlWarps) & 3;           // warp within its group
+    const int grp = (warp - kCtlWarps) >> 2;         // group: items n = grp, grp + 2, ...
+    const int gtid = (threadIdx.x - kCtlWarps * 32) & 127;   // thread within its group
     const int bar_id = 1 + grp;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     const int key_in_tile = q4 * 32 + lane;
@@ -671,12 +705,8 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       const int m = grp + 2 * (k - 1);
       item_vote(m, queue_item<VAR>(a, blockIdx.x + m * gridDim.x));
     }
-  }
-
-  __syncthreads();
-  if (warp == 1) {
-    ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, kTmemCols);
+    teardown();
+    return;
   }
 }
 
@@ -788,6 +818,15 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
 // columns), or 0 if the kernel cannot be resident. The answer depends only on the device and the
 // instantiation, so it is looked up once per (device, instantiation) and cached; the kernel's
 // shared-memory attribute is set at the same time.
+// The register split needs the launch to give every thread exactly kLaunchRegs registers (with
+// fewer, the epilogue's request could not be met and its warps would wait for ever): a kernel
+// built with another count is never launched (the grid is reported as not resident).
+template <typename K>
+bool launch_regs_ok(K kernel) {
+  cudaFuncAttributes fa{};
+  return cudaFuncGetAttributes(&fa, kernel) == cudaSuccess && fa.numRegs == kLaunchRegs;
+}
+
 template <int D, int N>
 int tc_grid() {
   using Lay = TcLayout<D, N>;
@@ -806,7 +845,7 @@ int tc_grid() {
           cudaSuccess &&
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vote_tc_kernel<D, N, false>, kThreadsTc, Lay::BYTES) ==
           cudaSuccess &&
-      per_sm > 0)
+      per_sm > 0 && launch_regs_ok(vote_tc_kernel<D, N, false>) && launch_regs_ok(vote_tc_kernel<D, N, true>))
     grid = sms;
   cache[dev].store(grid, std::memory_order_release);
   return grid > 0 ? grid : 0;

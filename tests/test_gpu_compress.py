@@ -238,3 +238,63 @@ def test_tied_block_cut_across_slices(dev, algo):
                         k_in=kf, v_in=vf, l_prefix=l_prefix, l_obs=lo, where="tied block")
     kept_ties = np.intersect1d(res["idx"][0, 0].cpu().numpy(), np.nonzero(p == tie)[0])
     assert kept_ties.size == budget - int(np.sum(p > tie)) and kept_ties[-1] > 2000   # past the first slice
+
+
+def _timing_event():
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)   # an event-record node under capture
+    except TypeError:
+        return torch.cuda.Event(enable_timing=True)
+
+
+def test_profiled_compress_records_stage_events(dev):
+    """snapkv_compress_profiled gives snapkv_compress's results and records the caller's events
+    around each stage, eagerly and as event-record nodes of a captured CUDA graph (replayed)."""
+    import ctypes
+    from kv_cache_compression_gb300 import snapkv
+    wl = synth.WORKLOADS[1].with_(heads=4)
+    q, k, v, _ = synth.device_inputs(wl, 0, 0, 1, wl.l_prompt, dev)
+    ref = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, budget=wl.budget, algo="tensor_core_cluster",
+                          want_vote=True)
+    params = snapkv.make_params(batch=1, heads=wl.heads, head_dim=wl.head_dim, l_obs=wl.l_obs,
+                                l_prompt=wl.l_prompt, pool_kernel=wl.pool_kernel, budget=wl.budget,
+                                algo="tensor_core_cluster")
+    cap = ref["cap"]
+    k_out, v_out = torch.zeros_like(ref["k_out"]), torch.zeros_like(ref["v_out"])
+    ln, idx, vote = torch.zeros_like(ref["len"]), torch.zeros_like(ref["idx"]), torch.zeros_like(ref["vote"])
+    ws = snapkv.new_workspace(snapkv.compress_workspace_size(params), dev)
+    stream = torch.cuda.Stream(dev)
+    evs = [_timing_event() for _ in range(8)]
+    with torch.cuda.stream(stream):
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    P = ctypes.c_void_p
+    arr = (ctypes.c_void_p * 8)(*[e.cuda_event for e in evs])
+
+    def call():
+        st = snapkv.lib().snapkv_compress_profiled(
+            ctypes.byref(params), P(q.data_ptr()), P(k.data_ptr()), P(v.data_ptr()), P(k_out.data_ptr()),
+            P(v_out.data_ptr()), cap, P(ln.data_ptr()), P(idx.data_ptr()), P(vote.data_ptr()), P(ws.data_ptr()),
+            ws.numel(), None, P(stream.cuda_stream), arr, 8)
+        assert st == snapkv.OK, snapkv.status_string(st)
+
+    def check():
+        for key, got in (("k_out", k_out), ("v_out", v_out), ("len", ln), ("idx", idx), ("vote", vote)):
+            assert torch.equal(got, ref[key]), key
+        stage = [evs[2 * s].elapsed_time(evs[2 * s + 1]) for s in range(4)]
+        assert stage[0] > 0 and stage[2] > 0, stage      # score (+ vote), top-k (+ gather)
+        assert all(t >= 0 for t in stage), stage
+
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    check()
+    for t in (k_out, v_out, ln, idx, vote):
+        t.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    graph.replay()
+    torch.cuda.synchronize()
+    check()

@@ -217,12 +217,14 @@ def compress(q_obs, k, v, *, pool_kernel, ratio_p=0.0, budget=0, scope="prompt_c
 
 def compress_varlen(q_obs, k, v, l_prompts, *, pool_kernel, ratio_p=0.0, budget=0, scope="prompt_causal",
                     algo="auto", cap=None, want_idx=True, want_vote=False, workspace=None, dev_status=None,
-                    stream=None, out=None):
+                    stream=None, out=None, k_out=None, v_out=None, len_out=None):
     """snapkv_compress_varlen: q_obs [B,H,L_obs,d]; k, v [B,H,L_max,d] padded, sequence b using its
     first l_prompts[b] rows (``v`` may be a pinned CPU tensor, as for compress). Returns k_out, v_out
     [B,H,cap,d], len [B], idx [B,H,k_max] (row b, h
     holds k_b indices), vote [B,H,L_max-L_obs] (if wanted), ks (per-sequence k) and the workspace.
-    ``out``: a previous call's result whose buffers (outputs and workspace) this call writes again."""
+    ``out``: a previous call's result whose buffers (outputs and workspace) this call writes again.
+    ``k_out``, ``v_out`` (contiguous [B,H,cap,d]) and ``len_out`` [B]: caller-owned outputs, e.g. a
+    slice of a larger cache (cap is then their third dimension)."""
     import numpy as np
     import torch
     B, H, L, d = k.shape
@@ -244,11 +246,19 @@ def compress_varlen(q_obs, k, v, l_prompts, *, pool_kernel, ratio_p=0.0, budget=
                                                         out["idx"], out["vote"])
         workspace = out["workspace"] if workspace is None else workspace
     else:
+        if k_out is not None:
+            cap = k_out.shape[2]
         if cap is None:
             cap = k_max + l_obs
-        k_out = torch.empty((B, H, cap, d), dtype=k.dtype, device=dev)
-        v_out = torch.empty_like(k_out)
-        len_out = torch.empty((B,), dtype=torch.int32, device=dev)
+        if k_out is None:
+            k_out = torch.empty((B, H, cap, d), dtype=k.dtype, device=dev)
+        if v_out is None:
+            v_out = torch.empty_like(k_out)
+        if len_out is None:
+            len_out = torch.empty((B,), dtype=torch.int32, device=dev)
+        for t in (k_out, v_out, len_out):
+            if not t.is_contiguous():
+                raise ValueError("tensors must be contiguous")
         idx_out = torch.full((B, H, max(k_max, 1)), -1, dtype=torch.int32, device=dev) if want_idx else None
         vote_out = torch.zeros((B, H, L - l_obs), dtype=torch.float32, device=dev) if want_vote else None
     need = int(lib().snapkv_compress_varlen_workspace_size(ctypes.byref(params), lens.ctypes.data_as(ctypes.c_void_p)))

@@ -355,3 +355,12 @@ def device_decode_tokens(wl: Workload, layer: int, step: int, seq0: int, nseq: i
                     tensor=t, seed=wl.seed, bf16=wl.bf16, stream=stream)
         outs.append(x)
     return tuple(outs)
+
+
+def device_decode_tokens_into(out, wl: Workload, layer: int, step: int, seq0: int, stream=0):
+    """Fill ``out`` ([3, n, H, d], contiguous, on the GPU) with the (q, k, v) of decode step ``step``
+    for sequences seq0..seq0+n-1: the values ``device_decode_tokens`` returns, written in place."""
+    n = out.shape[1]
+    for i, t in enumerate((T_QNEW, T_KNEW, T_VNEW)):
+        fill_device(out[i], n, wl.heads, 1, wl.head_dim, row0=step, seq0=seq0, head0=0, layer=layer,
+                    tensor=t, seed=wl.seed, bf16=wl.bf16, stream=stream)

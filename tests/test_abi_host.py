@@ -173,3 +173,15 @@ def test_status_strings(lib):
     assert sk.status_string(4) == "SNAPKV_ERR_CAPACITY"
     assert sk.status_string(4 | 16).startswith("SNAPKV_ERR_TIMEOUT")
     assert sk.status_string(-3) == "SNAPKV_ERR_UNKNOWN"
+
+
+def test_bench_decode_bytes_match_the_closed_form():
+    """The decode workload's algorithmic bytes: 2080 + t rows (t = 1..128) read per head-step, over
+    64 x 32 heads and 32 layers, is 274,496 rows x 2048 heads x 32 layers x 512 B = 9.21 TB, plus the
+    query, output and appended row (4 rows of d bf16 per head-step)."""
+    import bench
+    got = bench.decode_pass_bytes([2080] * 64, 32, 128, 128, 32)
+    rows = sum(2080 + t for t in range(1, 129))
+    assert rows == 274_496
+    assert got == (2 * rows + 4 * 128) * 64 * 32 * 32 * 128 * 2
+    assert abs(got / 9.21e12 - 1) < 2e-3

@@ -49,6 +49,12 @@ def _rank_main(rank: int, world: int, port: int):
         seqs = [None] * world
         dist.all_gather_object(seqs, seq)
         assert sorted(seqs) == list(range(world))
+        # a batch workload: rank r takes sequences r*B .. r*B + B - 1, disjoint across ranks
+        first = bench.replica_batch(rank, 8)
+        firsts = [None] * world
+        dist.all_gather_object(firsts, first)
+        spans = [set(range(f, f + 8)) for f in firsts]
+        assert not (spans[0] & spans[1]) and firsts[0] == 0
         wl = synth.WORKLOADS[0]
         hi = synth.host_head(wl, 0, seq, 0, l_prompt=wl.l_prompt, threads=1)
         ref = orc.compress_head(hi.q_obs, hi.k, hi.v, pool_kernel=wl.pool_kernel, ratio_p=wl.ratio_p)

@@ -287,16 +287,20 @@ SNAPKV_API snapkv_status snapkv_append_decode_attend(const void* q, const void* 
  * The pages have no counterpart to this entry point; it computes exactly what
  * snapkv_decode_attend computes, with the same arguments minus the workspace.
  *
- * It allocates nothing. Its scratch (the split partials and the per-head tickets) is a 16 MiB
- * array built into the library, which every GPU that loads the library holds until the process
- * exits. A problem needing more than that — 256-byte-rounded B*H*S*(d+2)*4 bytes of partials,
- * with S = ceil(cap/128) splits (longer splits once S would pass 512), plus B*H*4 bytes of
- * tickets — is rejected with SNAPKV_ERR_WORKSPACE before anything
- * is enqueued. The first call on a device looks up the array's device address (once per device,
- * with that device current), so make that first call before any stream capture. Every call
- * shares the one array and it keeps the last call's contents (the tickets are cleared on `stream`
- * at the start of each call), so calls that overlap on the GPU — on different streams, or from
- * different host threads — race and give wrong results: serialise them.
+ * It allocates nothing. Caches of up to 16384 rows per head take the cluster kernel, which keeps
+ * its partial results on chip and needs no scratch at all. Longer caches take the split kernel,
+ * whose scratch (the split partials and the per-head tickets) is a 16 MiB array built into the
+ * library, which every GPU that loads the library holds until the process exits. Such a problem
+ * needing more than that — 256-byte-rounded B*H*S*(d+2)*4 bytes of partials, with S = ceil(cap/128)
+ * splits (longer splits once S would pass 512), plus B*H*4 bytes of tickets — is rejected with
+ * SNAPKV_ERR_WORKSPACE before anything is enqueued. The first long-cache call on a device looks up
+ * the array's device address (with that device current) and caches it for the device's current
+ * context, so make that first call before any stream capture; a new context on the device (for
+ * example after cudaDeviceReset) makes the next call look it up again. All long-cache calls share the
+ * one array and it keeps the last call's contents (the tickets are cleared on `stream` at the start
+ * of each such call), so long-cache calls that overlap on the GPU — on different streams, or from
+ * different host threads — race and give wrong results: serialise them. Calls on caches of up to
+ * 16384 rows never touch the array and do not race.
  */
 SNAPKV_API snapkv_status snapkv_decode_attend_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                                       int64_t cap, const int32_t* len, void* out, int32_t batch,

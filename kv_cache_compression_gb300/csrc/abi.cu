@@ -588,7 +588,11 @@ snapkv_status snapkv_decode_attend_noalloc(const void* q, const void* k_cache, c
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || ((uintptr_t)len & 3u) ||
       ((uintptr_t)dev_status & 3u))
     return SNAPKV_ERR_INVALID_ARG;
-  if (decode_layout(batch, heads, head_dim, cap).total > kDecodeNoAllocScratchBytes) return SNAPKV_ERR_WORKSPACE;
+  // Only caches longer than the cluster kernel's limit take the split kernel, which keeps partials
+  // and tickets in the built-in array; shorter ones need no scratch at all.
+  if (cap > decode_fuses_append_max_cap() &&
+      decode_layout(batch, heads, head_dim, cap).total > kDecodeNoAllocScratchBytes)
+    return SNAPKV_ERR_WORKSPACE;
   DecodeJob job;
   job.batch = batch;
   job.heads = heads;

@@ -14,6 +14,8 @@
 // The cluster kernel can also take the step's append along (snapkv_append_decode_attend): the
 // CTA whose rows hold the new row writes it into the cache and into its shared-memory copy before
 // the attention reads it. The separate append kernel serves snapkv_append and longer caches.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "sm100_ptx.cuh"
@@ -492,7 +494,13 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(DecArgs a) {
 template <typename T, int D>
 cudaError_t launch_decode_cluster(const DecodeJob& job, const DecArgs& a) {
   const int64_t bh = (int64_t)job.batch * job.heads;
+  // CTAs per head: splitting a head's rows over a cluster cuts the latency of a small batch; once
+  // the heads alone give about two CTAs per SM, one CTA per head streams all its rows and skips the
+  // merge (2048 heads of 2208 rows: 8 CTAs per head 462 us, 1 CTA 319 us per launch; 256 heads of
+  // 850 rows: 7 CTAs 45 us, 1 CTA 22 us).
   int csize = (int)((job.cap + kSplitRows - 1) / kSplitRows);
+  const int64_t per_head = (int64_t)2 * device_sm_count() / (bh > 0 ? bh : 1);
+  if ((int64_t)csize > per_head) csize = (int)per_head;
   if (csize > kClMaxCtas) csize = kClMaxCtas;
   if (csize < 1) csize = 1;
   cudaLaunchConfig_t cfg = {};
@@ -560,20 +568,49 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};
 
-// Device address of the built-in scratch on the current device. The first call on a device looks
-// it up (the array's host-side name is only a stand-in, never a device address) and caches it.
+// Identifier of the calling thread's current context, unique for the life of the process (0 if
+// the driver cannot tell). A device's context is replaced by cudaDeviceReset or by a context the
+// caller makes current; the module, and with it the scratch array, is then loaded again at a new
+// address, so a cached address is only reused under the context it was looked up in.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the built-in scratch for the current device and context. The array's host-side
+// name is only a stand-in, never a device address: the first call on a device (and the first after
+// its context changed) looks the address up with cudaGetSymbolAddress and caches it.
 cudaError_t noalloc_scratch_address(void** out) {
   int dev = -1;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (!g_noalloc_addr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
     void* p = nullptr;
     err = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
     if (err != cudaSuccess) return err;
     g_noalloc_addr[dev] = p;
+    g_noalloc_ctx[dev] = current_context_id();   // the lookup made the context current if none was
   }
   *out = g_noalloc_addr[dev];
   return cudaSuccess;
@@ -581,6 +618,11 @@ cudaError_t noalloc_scratch_address(void** out) {
 }  // namespace
 
 cudaError_t launch_decode_noalloc(DecodeJob job) {
+  if (job.cap <= kClusterMaxCap) {   // the cluster kernel keeps its partials on chip: no scratch
+    job.partial = nullptr;
+    job.tickets = nullptr;
+    return launch_decode(job);
+  }
   const DecodeLayout L = decode_layout(job.batch, job.heads, job.head_dim, job.cap);
   if (L.total > kDecodeNoAllocScratchBytes) return cudaErrorInvalidValue;  // rejected earlier by the ABI
   void* base = nullptr;

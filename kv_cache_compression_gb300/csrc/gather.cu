@@ -4,6 +4,8 @@
 // K_c = [K[I]; K[L_prefix : L_prompt]] and V_c likewise, I ascending and different per head.
 // A bit-exact copy in 16-byte vectors; one thread per 16-byte piece of an output row, so a warp
 // moves contiguous 512-byte spans and every HBM sector it touches is used whole.
+#include <atomic>
+
 #include "snapkv_common.cuh"
 #include "snapkv_internal.h"
 
@@ -42,14 +44,24 @@ gather_window_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, u
 
 }  // namespace
 
+int device_sm_count() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];   // 0: not looked up yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 148;
+  int sms = cache[dev].load(std::memory_order_relaxed);
+  if (sms > 0) return sms;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+  cache[dev].store(sms, std::memory_order_relaxed);
+  return sms;
+}
+
 cudaError_t launch_gather(const CompressJob& job) {
   const int esize = job.dtype == SNAPKV_BF16 ? 2 : 4;
   const int vpr = job.head_dim * esize / 16;
   const int64_t rows_out = job.k_sel + job.l_obs;
   const int64_t total = (int64_t)job.batch * job.heads * rows_out * vpr;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sm_count();
   int64_t blocks = (total + 255) / 256;
   const int64_t cap_blocks = (int64_t)sms * 8;
   if (blocks > cap_blocks) blocks = cap_blocks;

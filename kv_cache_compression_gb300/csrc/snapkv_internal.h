@@ -136,6 +136,10 @@ struct HitRateJob {
 
 cudaError_t launch_hit_rate(const HitRateJob& job);
 
+// Streaming multiprocessors of the current device (looked up once per device; 148 if the query
+// fails). Launchers size their grids and cluster shapes with it.
+int device_sm_count();
+
 // Size of the built-in scratch array behind snapkv_decode_attend_noalloc.
 constexpr size_t kDecodeNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB
 // Decode attention with the split partials and tickets in the built-in scratch array

@@ -273,16 +273,3 @@ def kv_cache_bytes(batch: int, seq: int, layers: int, kv_heads: int, head_dim: i
                    elem_bytes: int) -> int:
     """[KVcache] 22.4: M_KV = 2 B S L H_KV d_h b (dense cache, keys and values)."""
     return 2 * batch * seq * layers * kv_heads * head_dim * elem_bytes
-
-
-def round_bf16(x: np.ndarray) -> np.ndarray:
-    """Round float64 values to the nearest bf16 (ties to even), returned as float64.
-
-    Used only to compare bf16 outputs: float64 -> float32 (nearest) -> bf16 (nearest even).
-    The double rounding can differ from a direct float64 -> bf16 rounding by one bf16 ulp only
-    on exact float32 ties, which the 2e-3 decode tolerance absorbs.
-    """
-    f = np.asarray(x, dtype=np.float64).astype(np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32).astype(np.float64)

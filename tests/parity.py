@@ -70,3 +70,44 @@ def to_numpy_f32(t):
     """A torch tensor (bf16 or fp32, any device) as float32 numpy values."""
     import torch
     return t.detach().to("cpu").to(torch.float32).numpy()
+
+
+# Canary guard bands: output buffers are pre-filled with a NaN bit pattern that no kernel writes, so
+# that every row, index or vote entry the library promises to leave untouched can be checked after
+# the call (rows past k + L_obs of the cache, indices past a sequence's own k, votes past its own
+# L_prefix).
+CANARY_BF16 = 0x7FC1            # bf16 quiet NaN with a payload
+CANARY_F32 = 0x7FC00BAD         # fp32 quiet NaN with a payload
+CANARY_I32 = -0x5EED
+
+
+def canary_like(shape, dtype, device):
+    """A tensor of `shape` and `dtype` (bf16, fp32 or int32) filled with the canary bit pattern."""
+    import torch
+    if dtype == torch.bfloat16:
+        return torch.full(shape, CANARY_BF16, dtype=torch.int16, device=device).view(torch.bfloat16)
+    if dtype == torch.float32:
+        return torch.full(shape, CANARY_F32, dtype=torch.int32, device=device).view(torch.float32)
+    if dtype == torch.int32:
+        return torch.full(shape, CANARY_I32, dtype=torch.int32, device=device)
+    raise TypeError(dtype)
+
+
+def assert_canary(t, where=""):
+    """Every element of `t` still holds the canary bit pattern."""
+    import torch
+    if t.numel() == 0:
+        return
+    if t.dtype == torch.bfloat16:
+        ok = bool((t.view(torch.int16) == CANARY_BF16).all())
+    elif t.dtype == torch.float32:
+        ok = bool((t.view(torch.int32) == CANARY_F32).all())
+    else:
+        ok = bool((t == CANARY_I32).all())
+    assert ok, f"{where}: an element the call must leave untouched was written"
+
+
+def bf16_bits(t):
+    """A bf16 torch tensor's bit patterns as a uint16 numpy array (host)."""
+    import torch
+    return t.detach().contiguous().view(torch.int16).to("cpu").numpy().view(np.uint16)

@@ -12,7 +12,8 @@ import torch
 
 import synth
 from oracle import snapkv_oracle as orc
-from tests.parity import check_compress_head, to_numpy_f32
+from tests import oracle_pool
+from tests.parity import assert_canary, bf16_bits, canary_like, check_compress_head, to_numpy_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -31,13 +32,20 @@ def _run_workload(dev, wl, layer=0, seq0=0, nseq=None, l_prompt=None, heads=None
     L = l_prompt if l_prompt is not None else wl.prompt_lengths()[seq0]
     q, k, v, _ = synth.device_inputs(wl, layer, seq0, nseq, L, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    l_prefix = L - wl.l_obs
+    ksel = orc.kept_slots(l_prefix, ratio_p=wl.ratio_p, budget=wl.budget)
+    R = ksel + wl.l_obs
+    cap = R + 3   # rows past k + L_obs are a canary guard band the call must leave untouched
+    k_out = canary_like((nseq, wl.heads, cap, wl.head_dim), k.dtype, dev)
+    v_out = canary_like((nseq, wl.heads, cap, wl.head_dim), k.dtype, dev)
     res = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, ratio_p=wl.ratio_p, budget=wl.budget, scope=scope,
-                          algo=algo, want_vote=True, dev_status=status)
+                          algo=algo, want_vote=True, dev_status=status, cap=cap, k_out=k_out, v_out=v_out)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    l_prefix = L - wl.l_obs
-    ksel = res["k"]
+    assert res["k"] == ksel
     assert res["len"].cpu().tolist() == [ksel + wl.l_obs] * nseq
+    assert_canary(k_out[:, :, R:], "k_out rows past k + L_obs")
+    assert_canary(v_out[:, :, R:], "v_out rows past k + L_obs")
     excused = 0
     for b in range(nseq):
         for h in (heads if heads is not None else range(wl.heads)):
@@ -67,21 +75,102 @@ def test_llama_layer_every_head(dev, algo):
     print(f"boundary-excused indices ({algo}): {excused}")
 
 
-@pytest.mark.parametrize("algo", ["tensor_core", "simt"])
-def test_long_context_sampled_heads(dev, algo):
-    _run_workload(dev, synth.WORKLOADS[3], heads=[0, 13, 31], algo=algo)
+def _compress_jobs(wl, res, layer, seq0, units, L, scope="prompt_causal"):
+    """Oracle-pool jobs for the (sequence offset b, head h) units of one compression result."""
+    idx, vote = res["idx"].cpu().numpy(), res["vote"].cpu().numpy()
+    R = res["k"] + wl.l_obs
+    kc, vc = bf16_bits(res["k_out"][:, :, :R]), bf16_bits(res["v_out"][:, :, :R])
+    return [dict(wl=wl, layer=layer, seq=seq0 + b, head=h, l_prompt=L, scope=scope, idx=idx[b, h], kc_bits=kc[b, h],
+                 vc_bits=vc[b, h], vote=vote[b, h], where=f"layer {layer} seq {seq0 + b} head {h}") for b, h in units]
+
+
+def _pool_verdict(results):
+    errors = [f"{w}: {e}" for w, _, e in results if e is not None]
+    assert not errors, "\n".join(errors[:5]) + (f"\n... {len(errors)} heads failed" if len(errors) > 5 else "")
+    return sum(r for _, r, _ in results)
+
+
+def test_long_context_every_head(dev):
+    """The long-context workload (131072 keys, L_obs 64, K_pool 13, budget 4096) on every head, in the
+    launch configuration of the default (streaming tensor-core) path."""
+    from kv_cache_compression_gb300 import snapkv
+    wl = synth.WORKLOADS[3]
+    L = wl.l_prompt
+    q, k, v, _ = synth.device_inputs(wl, 0, 0, 1, L, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, budget=wl.budget, want_vote=True, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    jobs = _compress_jobs(wl, res, 0, 0, [(0, h) for h in range(wl.heads)], L)
+    del q, k, v
+    excused = _pool_verdict(oracle_pool.run(oracle_pool.check_compress_job, jobs))
+    print(f"long context: {len(jobs)} heads, {excused} boundary-excused indices")
+
+
+def test_long_context_sampled_heads_simt(dev):
+    _run_workload(dev, synth.WORKLOADS[3], heads=[0, 13, 31], algo="simt")
 
 
 def test_llama_layer_prefix_only_tensor_core(dev):
     _run_workload(dev, synth.WORKLOADS[1].with_(heads=8), scope="prefix_only", algo="tensor_core")
 
 
-def test_prefill_32_layers_sampled(dev):
+def prefill_parity_units(seed=0xC2):
+    """The 32-layer prefill's parity coverage: every (sequence, head) of layers 0 and 31, plus 64 seeded
+    (layer, sequence, head) units drawn from all 32 layers; layer -> sorted (sequence, head) list."""
+    rng = np.random.default_rng(seed)
+    units = {0: {(b, h) for b in range(8) for h in range(32)}, 31: {(b, h) for b in range(8) for h in range(32)}}
+    for u in rng.choice(32 * 8 * 32, size=64, replace=False):
+        layer, b, h = int(u // 256), int((u // 32) % 8), int(u % 32)
+        units.setdefault(layer, set()).add((b, h))
+    return {layer: sorted(bh) for layer, bh in sorted(units.items())}
+
+
+def test_prefill_32_layers_parity_coverage(dev):
+    """The 32-layer batch-8 prefill in the benchmark's launch configuration (one call per layer over
+    B8 x 32 heads, p = 0.05, K with per-channel scales): every head of layers 0 and 31 and 64 seeded
+    units from the other layers against the oracle, and the cache rows past k + L_obs untouched."""
+    from kv_cache_compression_gb300 import snapkv
     wl = synth.WORKLOADS[2]
-    rng = np.random.default_rng(2)
-    for layer in (0, 31, int(rng.integers(1, 31))):
-        _run_workload(dev, wl, layer=layer, seq0=int(rng.integers(0, 8)), nseq=1,
-                      heads=sorted(rng.choice(32, 3, replace=False).tolist()))
+    L, B, H = wl.l_prompt, wl.batch, wl.heads
+    ksel = orc.kept_slots(L - wl.l_obs, ratio_p=wl.ratio_p)
+    R = ksel + wl.l_obs
+    cap = R + 1
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    jobs = []
+    units = prefill_parity_units()
+    assert sum(len(u) for u in units.values()) >= 512 + 60
+    for layer, bhs in units.items():
+        q, k, v, _ = synth.device_inputs(wl, layer, 0, B, L, dev)
+        k_out = canary_like((B, H, cap, wl.head_dim), k.dtype, dev)
+        v_out = canary_like((B, H, cap, wl.head_dim), k.dtype, dev)
+        res = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, ratio_p=wl.ratio_p, cap=cap, k_out=k_out,
+                              v_out=v_out, want_vote=True, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0 and res["k"] == ksel
+        assert res["len"].cpu().tolist() == [R] * B
+        assert_canary(k_out[:, :, R:], f"layer {layer}: k_out row R")
+        assert_canary(v_out[:, :, R:], f"layer {layer}: v_out row R")
+        jobs += _compress_jobs(wl, res, layer, 0, bhs, L)
+        del q, k, v, res
+    excused = _pool_verdict(oracle_pool.run(oracle_pool.check_compress_job, jobs))
+    print(f"32-layer prefill: {len(jobs)} heads over {len(units)} layers, {excused} boundary-excused indices")
+
+
+@pytest.mark.parametrize("batch,l_prompt", [(16, 4096), (4, 8192), (2, 12000)])
+def test_large_batch_cluster_shapes(dev, batch, l_prompt):
+    """Batches that give the top-k kernel one, four and six CTAs per head (its cluster shrinks as the
+    heads alone fill the GPU), with the decode-shaped budget rule; every head against the oracle."""
+    from kv_cache_compression_gb300 import snapkv
+    wl = synth.WORKLOADS[2].with_(batch=batch, l_prompt=l_prompt, layers=1)
+    q, k, v, _ = synth.device_inputs(wl, 5, 0, batch, l_prompt, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, ratio_p=wl.ratio_p, want_vote=True, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    jobs = _compress_jobs(wl, res, 5, 0, [(b, h) for b in range(batch) for h in range(wl.heads)], l_prompt)
+    del q, k, v
+    _pool_verdict(oracle_pool.run(oracle_pool.check_compress_job, jobs))
 
 
 def test_ragged_prompts_sampled(dev):

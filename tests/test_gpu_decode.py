@@ -269,3 +269,106 @@ def test_full_16k_cache_decode_sampled(dev, extra):
     for b, h in [(0, 0), (1, 17), (1, 31)]:
         ref = orc.decode_attend(to_numpy_f32(qn[b, h]), to_numpy_f32(kc[b, h, :n]), to_numpy_f32(vc[b, h, :n]))
         check_decode(o[b, h], ref, True, where=f"b{b} h{h} n{n}")
+
+
+def test_prefill_step_launch_configuration(dev):
+    """The 32-layer prefill benchmark's per-layer step as it is timed: one layer of B8 x 32 heads
+    compressed (p = 0.05) into a cache of capacity k + L_obs + 1, then one fused decode step filling its
+    last row (256 heads: one CTA per head); every head's output against the oracle's decode over that
+    head's cache rows, the appended rows and the new lengths."""
+    from kv_cache_compression_gb300 import snapkv
+    wl = synth.WORKLOADS[2]
+    B, H, L = wl.batch, wl.heads, wl.l_prompt
+    q, k, v, _ = synth.device_inputs(wl, 7, 0, B, L, dev)
+    ksel = orc.kept_slots(L - wl.l_obs, ratio_p=wl.ratio_p)
+    cap = ksel + wl.l_obs + 1
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, ratio_p=wl.ratio_p, cap=cap, dev_status=status)
+    del q, k, v
+    qn, kn, vn = synth.device_decode_tokens(wl, 7, 0, 0, B, dev)
+    out, len_next = snapkv.append_decode_attend(qn, kn, vn, res["k_out"], res["v_out"], res["len"],
+                                                dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert res["len"].cpu().tolist() == [cap - 1] * B and len_next.cpu().tolist() == [cap] * B
+    o = to_numpy_f32(out)
+    kc, vc = to_numpy_f32(res["k_out"]), to_numpy_f32(res["v_out"])
+    for b in range(B):
+        for h in range(H):
+            qh, kh, vh = synth.host_decode_token(wl, 7, b, h, 0)
+            assert np.array_equal(kc[b, h, cap - 1], kh) and np.array_equal(vc[b, h, cap - 1], vh)
+            check_decode(o[b, h], orc.decode_attend(qh, kc[b, h], vc[b, h]), True, where=f"seq {b} head {h}")
+
+
+def decode_parity_triples(seed=0xC4):
+    """64 seeded (sequence, layer, head) triples of the decode workload; layer -> [(sequence, head)]."""
+    rng = np.random.default_rng(seed)
+    by_layer = {}
+    for u in rng.choice(64 * 32 * 32, size=64, replace=False):
+        seq, layer, head = int(u // 1024), int((u // 32) % 32), int(u % 32)
+        by_layer.setdefault(layer, []).append((seq, head))
+    return dict(sorted(by_layer.items()))
+
+
+def test_decode_workload_64_triples_through_128_steps(dev):
+    """The compressed-decode workload in the benchmark's launch configuration: per layer, the 64 ragged
+    prompts compressed (budget 2048, one snapkv_compress_varlen call per 16 sequences) into a
+    [64, 32, 2208, 128] cache, then 128 fused append + attention steps over all 64 x 32 heads. For 64
+    seeded (sequence, layer, head) triples the compression and every step's output are checked
+    against the oracle, which re-simulates that head from its own inputs through all 128 steps; the
+    cache rows past the compressed length stay untouched until the steps write them."""
+    from kv_cache_compression_gb300 import snapkv
+    from tests import oracle_pool
+    from tests.parity import assert_canary, bf16_bits, canary_like
+    wl = synth.WORKLOADS[4]
+    B, H, d, lo, steps = wl.batch, wl.heads, wl.head_dim, wl.l_obs, wl.decode_steps
+    lengths = wl.prompt_lengths()
+    cap = wl.budget + lo + steps
+    R = wl.budget + lo
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = snapkv.new_workspace(snapkv.decode_workspace_size(B, H, d, cap), dev)
+    jobs = []
+    for layer, units in decode_parity_triples().items():
+        kc = canary_like((B, H, cap, d), torch.bfloat16, dev)
+        vc = canary_like((B, H, cap, d), torch.bfloat16, dev)
+        lens = torch.zeros((2, B), dtype=torch.int32, device=dev)
+        idx = torch.empty((B, H, wl.budget), dtype=torch.int32, device=dev)
+        for c0 in range(0, B, 16):
+            ls = lengths[c0:c0 + 16]
+            q, k, v = synth.device_inputs_padded(wl, layer, c0, ls, dev, pad_value=0.0)
+            res = snapkv.compress_varlen(q, k, v, ls, pool_kernel=wl.pool_kernel, budget=wl.budget,
+                                         k_out=kc[c0:c0 + 16], v_out=vc[c0:c0 + 16], len_out=lens[0, c0:c0 + 16],
+                                         dev_status=status)
+            idx[c0:c0 + 16].copy_(res["idx"])
+            del q, k, v
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert lens[0].cpu().tolist() == [R] * B
+        assert_canary(kc[:, :, R:], f"layer {layer}: cache rows past the compressed length")
+        sel_b = torch.tensor([s for s, _ in units], device=dev)
+        sel_h = torch.tensor([h for _, h in units], device=dev)
+        kc_bits, vc_bits = bf16_bits(kc[sel_b, sel_h, :R]), bf16_bits(vc[sel_b, sel_h, :R])
+        idx_sel = idx[sel_b, sel_h].cpu().numpy()
+        outs = torch.empty((steps, len(units), d), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((B, H, d), dtype=torch.bfloat16, device=dev)
+        for t in range(steps):
+            qn, kn, vn = synth.device_decode_tokens(wl, layer, t, 0, B, dev)
+            snapkv.append_decode_attend(qn, kn, vn, kc, vc, lens[t % 2], lens[(t + 1) % 2], out=out, workspace=ws,
+                                        dev_status=status)
+            outs[t] = out[sel_b, sel_h]
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert lens[steps % 2].cpu().tolist() == [cap] * B
+        out_bits = bf16_bits(outs)
+        for i, (s, h) in enumerate(units):
+            jobs.append(dict(wl=wl, layer=layer, seq=s, head=h, l_prompt=lengths[s], idx=idx_sel[i],
+                             kc_bits=kc_bits[i], vc_bits=vc_bits[i], out_bits=out_bits[:, i],
+                             where=f"seq {s} (L {lengths[s]}) layer {layer} head {h}"))
+        del kc, vc
+    results = oracle_pool.run(oracle_pool.check_decode_run_job, jobs)
+    errors = [f"{w}: {e}" for w, _, e in results if e is not None]
+    assert not errors, "\n".join(errors[:5])
+    assert len(jobs) == 64
+    worst = max(r[1] for _, r, _ in results)
+    print(f"decode workload: 64 triples x 128 steps, worst |o - o_ref| {worst:.2e}, "
+          f"{sum(r[0] for _, r, _ in results)} boundary-excused indices")

@@ -1,4 +1,4 @@
-// Max-pool + top-k + ascending compaction, one CTA per (sequence, head).
+// Max-pool + top-k + ascending compaction (+ the gather of the kept rows), per (sequence, head).
 //
 // SnapKV explainer ("論文解説: SnapKV"), sections クラスタリングによる文脈保持 and 投票メカニズム:
 // P_j = max of the vote C over |j' - j| <= K_pool / 2 (clipped to the prefix, i.e. -inf padding),
@@ -9,13 +9,16 @@
 // pattern, and how many copies of tau to keep; one ordered compaction pass then keeps every
 // P_j > tau and the lowest-index copies of tau, writing the indices ascending.
 //
-// Two kernels: for prefixes up to kClusterMaxPrefix a cluster of up to 8 CTAs shares a head, each
-// CTA holding a contiguous slice of P in shared memory; the slices' histograms are summed through
-// distributed shared memory and every CTA locates the same digit; the compaction offsets of the
-// slices are exchanged the same way. That kernel also does the gather of the section アルゴリズム
-// (K_c = [K[I]; K[L_prefix:]], V_c likewise): a CTA's kept indices are a contiguous block of the
-// ascending output, so it copies its own kept rows, and a share of the window rows. Longer
-// prefixes take one CTA per head with P in global memory, followed by the separate gather kernel.
+// Two kernels, chosen by the prefix length:
+//   * prefixes up to kClusterMaxPrefix: a cluster of up to 8 CTAs per head (fewer, down to one, when
+//     the batch alone fills the GPU); each CTA holds a contiguous slice of P in shared memory; the
+//     slices' histograms are summed through distributed shared memory and every CTA locates the same
+//     digit; the compaction offsets of the slices are exchanged the same way. The kernel also does
+//     the gather of the section アルゴリズム (K_c = [K[I]; K[L_prefix:]], V_c likewise): a CTA's kept
+//     indices are a contiguous block of the ascending output, so it copies its own kept rows, and a
+//     share of the window rows;
+//   * longer prefixes: one CTA per head with P in global memory, followed by the separate gather
+//     kernel.
 #include "sm100_ptx.cuh"
 #include "snapkv_common.cuh"
 #include "snapkv_internal.h"
@@ -209,6 +212,52 @@ constexpr int kSumWords = 2 * kMaxBins;
 
 __host__ __device__ constexpr int round4(int x) { return (x + 3) & ~3; }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
+// Stages hn (<= kPoolChunk + 1024) vote values starting at prefix position h0 into buf, -inf outside
+// [0, L): every load of the chunk is issued before the first store, so the chunk costs one memory
+// round trip rather than one per value.
+constexpr int kStageLoads = (kPoolChunk + 1024 + 511) / 512;
+__device__ __forceinline__ void stage_vote(float* buf, const float* c, int h0, int hn, int L) {
+  float x[kStageLoads];
+#pragma unroll
+  for (int i = 0; i < kStageLoads; ++i) {
+    const int q = (int)threadIdx.x + i * (int)blockDim.x;
+    const int j = h0 + q;
+    x[i] = (q < hn && j >= 0 && j < L) ? __ldcg(c + j) : -INFINITY;
+  }
+#pragma unroll
+  for (int i = 0; i < kStageLoads; ++i) {
+    const int q = (int)threadIdx.x + i * (int)blockDim.x;
+    if (q < hn) buf[q] = x[i];
+  }
+}
+
+// Max over the staged window buf[j .. j + 2 radius] (the pool of position j); the explainer's
+// presets use kernels of 5 to 13, so those take an unrolled path.
+__device__ __forceinline__ float window_max(const float* buf, int j, int radius) {
+  float m = buf[j];
+  switch (radius) {
+    case 2:
+#pragma unroll
+      for (int q = 1; q <= 4; ++q) m = fmaxf(m, buf[j + q]);
+      break;
+    case 3:
+#pragma unroll
+      for (int q = 1; q <= 6; ++q) m = fmaxf(m, buf[j + q]);
+      break;
+    case 6:
+#pragma unroll
+      for (int q = 1; q <= 12; ++q) m = fmaxf(m, buf[j + q]);
+      break;
+    default:
+      for (int q = 1; q <= 2 * radius; ++q) m = fmaxf(m, buf[j + q]);
+  }
+  return m;
+}
+
 // One cluster per (sequence, head); CTA `rank` of the cluster owns P[rank * slice, ...).
 //
 // Each CTA keeps a copy of the cluster-wide histogram. In a radix pass every CTA histograms its
@@ -236,6 +285,90 @@ struct GatherArgs {
   } var;
 };
 
+// One step of the radix select: in the complete histogram `s` (nb bins) of the values that match
+// the digits found so far, the bin holding the krem-th largest value, counted from the top bin.
+// Writes the bin, the count of values in higher bins, whether the bin's values are all kept and the
+// bin's count to the shared outputs; every thread of the CTA must call it, and a barrier must come
+// before the outputs are read. Thread t holds the four bins of group t counted from the top; a
+// block scan gives the values in higher groups.
+__device__ __forceinline__ void find_digit(const uint32_t* s, int nb, uint32_t krem, uint32_t* sh_warp,
+                                           uint32_t* sh_digit, uint32_t* sh_above, uint32_t* sh_full,
+                                           uint32_t* sh_bin) {
+  const int tid = threadIdx.x;
+  const int ngroups = nb / 4;   // <= kCThreads
+  const int grp = ngroups - 1 - tid;
+  uint4 g4 = make_uint4(0, 0, 0, 0);
+  if (tid < ngroups) g4 = *reinterpret_cast<const uint4*>(s + 4 * grp);
+  const uint32_t cnt = g4.x + g4.y + g4.z + g4.w;
+  const uint32_t above = cta_exclusive_scan(cnt, sh_warp);
+  if (tid < ngroups && above < krem && krem <= above + cnt) {
+    uint32_t acc = above;
+    const uint32_t hb[4] = {g4.w, g4.z, g4.y, g4.x};   // bins 4 grp + 3 .. 4 grp
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (acc + hb[q] >= krem) {
+        *sh_digit = (uint32_t)(4 * grp + 3 - q);
+        *sh_above = acc;
+        *sh_full = acc + hb[q] == krem ? 1u : 0u;   // the digit's bin is kept whole
+        *sh_bin = hb[q];
+        break;
+      }
+      acc += hb[q];
+    }
+  }
+}
+
+// Gather of the section アルゴリズム for one CTA's share of a head (K and V together): the CTA's kept
+// prefix rows, which take cache rows p0 .. p0 + n_rows - 1, then the window rows rank, rank + csize,
+// ... of the L_obs window. The kept positions are read from `kept` in shared memory when the list
+// fit there, else (kept == nullptr) from the head's index row, which this CTA wrote before the
+// barrier that precedes the call. 16-byte pieces, four rows' worth of loads in flight per thread; the
+// destinations are recomputed for the stores rather than held in registers across the loads, which
+// keeps the kernels free of spills.
+__device__ __forceinline__ void gather_rows(const GatherArgs& g, int64_t bh, uint32_t rank, uint32_t csize,
+                                            const uint32_t* kept, const int32_t* idx, uint32_t p0,
+                                            uint32_t n_rows, int64_t l_prefix, int64_t k_sel) {
+  const int tid = threadIdx.x;
+  const int vpr = g.vpr;
+  const uint4* kin = g.k + bh * g.kv_stride * vpr;
+  const uint4* vin = g.v + bh * g.kv_stride * vpr;
+  uint4* kout = g.k_out + bh * g.cap * vpr;
+  uint4* vout = g.v_out + bh * g.cap * vpr;
+  const int n_win = (g.l_obs - (int)rank + (int)csize - 1) / (int)csize;   // window rows of this CTA
+  const int64_t items = ((int64_t)n_rows + n_win) * vpr;
+  constexpr int U = 4;
+  const int vsh = __ffs(vpr) - 1;   // 16-byte pieces per row: 8, 16 or 32
+  for (int64_t base = tid; base < items; base += (int64_t)U * blockDim.x) {
+    uint4 kv[U], vv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t it = base + (int64_t)u * blockDim.x;
+      if (it < items) {
+        const int64_t row = it >> vsh;
+        const int c = (int)(it & (vpr - 1));
+        int64_t src;
+        if (row < (int64_t)n_rows)
+          src = kept ? (int64_t)kept[row] : (int64_t)__ldcg(idx + p0 + row);
+        else
+          src = l_prefix + (int64_t)rank + (row - n_rows) * csize;
+        kv[u] = ld_stream_v4(kin + src * vpr + c);
+        vv[u] = ld_stream_v4(vin + src * vpr + c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t it = base + (int64_t)u * blockDim.x;
+      if (it < items) {
+        const int64_t row = it >> vsh;
+        const int c = (int)(it & (vpr - 1));
+        const int64_t out = row < (int64_t)n_rows ? (int64_t)p0 + row : k_sel + (int64_t)rank + (row - n_rows) * csize;
+        kout[out * vpr + c] = kv[u];
+        vout[out * vpr + c] = vv[u];
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kCThreads, 2)   // two CTAs per SM (a 32-head layer in one wave)
 pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ idx_all, int64_t l_prefix,
                          int radius, int64_t k_sel, int slice, GatherArgs g) {
@@ -248,7 +381,7 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   // (the layout above is sized for the largest slice; a ragged batch's shorter sequences use less)
   uint32_t* sh_warp = sums + kSumWords;                      // [32]
   uint32_t* counts = sh_warp + 32;                           // [8 + 1] packed (greater << 16 | equal) per slice
-  __shared__ uint32_t sh_digit, sh_above, sh_full;
+  __shared__ uint32_t sh_digit, sh_above, sh_full, sh_bin;
 
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t rank = ptx::cluster_rank(), csize = ptx::cluster_size();
@@ -264,9 +397,16 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   const int L = (int)l_prefix;
   const int j0 = min(L, (int)rank * slice), j1 = min(L, j0 + slice);
   const int n = j1 - j0;
+  // The vote was written by the score kernel just before, but much of it has left L2 behind the
+  // keys streamed since: every 128-byte line of the slice is requested at once.
+  for (int q = tid * 32; q < n; q += kCThreads * 32) prefetch_l2(c + j0 + q);
 
-  for (int b = tid; b < kSumWords; b += kCThreads) sums[b] = 0u;
-  ptx::cluster_arrive();   // this CTA's cluster histograms are clear (waited for before the first add)
+  // A head on one CTA reads its own histograms and skips every cluster exchange.
+  const bool alone = csize == 1;
+  if (!alone) {
+    for (int b = tid; b < kSumWords; b += kCThreads) sums[b] = 0u;
+    ptx::cluster_arrive();   // this CTA's cluster histograms are clear (waited for before the first add)
+  }
 
   // Max pool of the slice, kPoolChunk values at a time: the vote (L2-resident) with its halo is
   // staged in shared memory by coalesced independent loads, -inf outside the prefix; then each P_j
@@ -275,16 +415,9 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
   for (int ch0 = 0; ch0 < n; ch0 += kPoolChunk) {
     const int cn = min(kPoolChunk, n - ch0);
     const int h0 = j0 + ch0 - radius, hn = cn + 2 * radius;
-    for (int q = tid; q < hn; q += kCThreads) {
-      const int j = h0 + q;
-      cbuf[q] = (j >= 0 && j < L) ? __ldcg(c + j) : -INFINITY;
-    }
+    stage_vote(cbuf, c, h0, hn, L);
     __syncthreads();
-    for (int j = tid; j < cn; j += kCThreads) {
-      float m = cbuf[j];
-      for (int q = 1; q <= 2 * radius; ++q) m = fmaxf(m, cbuf[j + q]);
-      pbits[ch0 + j] = __float_as_uint(m);
-    }
+    for (int j = tid; j < cn; j += kCThreads) pbits[ch0 + j] = __float_as_uint(window_max(cbuf, j, radius));
     __syncthreads();   // the next chunk, and the histogram below, reuse the staging buffer
   }
   uint32_t prefix = 0, mask = 0, krem = (uint32_t)k_sel;
@@ -299,36 +432,18 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
       warp_hist_add(hist, (u >> shift) & (uint32_t)(nb - 1), j < n && (u & mask) == prefix);
     }
     __syncthreads();
-    if (pass == 0) ptx::cluster_wait();
-    for (int b = tid; b < nb; b += kCThreads) {
-      const uint32_t v = hist[b];
-      if (v != 0u)
-        for (uint32_t r = 0; r < csize; ++r) ptx::dsmem_add_u32(ptx::map_rank(s + b, r), v);
-    }
-    ptx::cluster_sync();   // every slice's bins have been added into every copy
-
-    // Thread t holds the four bins of group t counted from the top; a block scan gives the values
-    // in higher groups, and the group where that count first reaches k resolves the digit.
-    const int ngroups = nb / 4;   // <= kCThreads
-    const int g = ngroups - 1 - tid;
-    uint4 g4 = make_uint4(0, 0, 0, 0);
-    if (tid < ngroups) g4 = *reinterpret_cast<const uint4*>(s + 4 * g);
-    const uint32_t cnt = g4.x + g4.y + g4.z + g4.w;
-    const uint32_t above = cta_exclusive_scan(cnt, sh_warp);
-    if (tid < ngroups && above < krem && krem <= above + cnt) {
-      uint32_t acc = above;
-      const uint32_t hb[4] = {g4.w, g4.z, g4.y, g4.x};   // bins 4g+3 .. 4g
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (acc + hb[q] >= krem) {
-          sh_digit = (uint32_t)(4 * g + 3 - q);
-          sh_above = acc;
-          sh_full = acc + hb[q] == krem ? 1u : 0u;   // the digit's bin is kept whole
-          break;
-        }
-        acc += hb[q];
+    const uint32_t* whole = hist;   // the head's histogram
+    if (!alone) {
+      if (pass == 0) ptx::cluster_wait();
+      for (int b = tid; b < nb; b += kCThreads) {
+        const uint32_t v = hist[b];
+        if (v != 0u)
+          for (uint32_t r = 0; r < csize; ++r) ptx::dsmem_add_u32(ptx::map_rank(s + b, r), v);
       }
+      ptx::cluster_sync();   // every slice's bins have been added into every copy
+      whole = s;
     }
+    find_digit(whole, nb, krem, sh_warp, &sh_digit, &sh_above, &sh_full, &sh_bin);
     __syncthreads();
     prefix |= sh_digit << shift;
     mask |= (uint32_t)(nb - 1) << shift;
@@ -336,35 +451,49 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
     // When every value with the digits found so far is kept, the lower digits cannot change the
     // selection: stop (every CTA reads the same histogram, so all stop at the same pass).
     if (sh_full) break;
-    if (pass == 0)   // cleared before this CTA arrives at the next pass's barrier
+    if (pass == 0 && !alone)   // cleared before this CTA arrives at the next pass's barrier
       for (int b = tid; b < nb; b += kCThreads) s[b] = 0u;
   }
   // Selection: every value whose decided digits exceed tau's, plus the lowest-index need_eq of
   // those equal to tau's (all of them when the select stopped early).
   const uint32_t tau = prefix, need_eq = krem;
 
-  // Ordered compaction: thread = contiguous run of the slice; slices in rank order. A slice holds
-  // fewer than 2^16 values, so its (greater, equal) counts scan as one packed word; each CTA
-  // stores its total into the later slices' CTAs.
-  const int per = (n + kCThreads - 1) / kCThreads;
-  const int a0 = min(n, tid * per), a1 = min(n, a0 + per);
-  uint32_t gt = 0, eq = 0;
-  for (int j = a0; j < a1; ++j) {
-    const uint32_t u = pbits[j] & mask;
-    gt += u > tau;
-    eq += u == tau;
+  // Ordered compaction, warp-ordered: warp w owns the contiguous segment [w * seg, (w + 1) * seg) of
+  // the slice (seg a multiple of 32) and reads it 32 consecutive values at a time, so lane l reads
+  // word base + l (no bank conflicts); ballots give each value's rank among the greater and equal
+  // values before it. Slices are in rank order; a slice holds fewer than 2^16 values, so its
+  // (greater, equal) counts travel as one packed word, and each CTA stores its total into the later
+  // slices' CTAs.
+  const int warp = tid >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  const int seg = ((n + kCWarps * 32 - 1) / (kCWarps * 32)) * 32;
+  const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
+  uint32_t w_gt = 0, w_eq = 0;
+  for (int base = s0; base < s1; base += 32) {   // warp-uniform trip count
+    const int j = base + lane;
+    const uint32_t u = j < s1 ? (pbits[j] & mask) : 0u;
+    w_gt += __popc(__ballot_sync(0xffffffffu, j < s1 && u > tau));
+    w_eq += __popc(__ballot_sync(0xffffffffu, j < s1 && u == tau));
   }
-  const uint32_t packed = (gt << 16) | eq;
-  const uint32_t packed_in = cta_exclusive_scan(packed, sh_warp);
-  const uint32_t cta_total = packed_in + packed;   // valid in the last thread
-  if (tid == kCThreads - 1) {
+  if (lane == 0) sh_warp[warp] = (w_gt << 16) | w_eq;
+  __syncthreads();
+  uint32_t packed_in = 0, cta_total = 0;   // this warp's exclusive prefix, the CTA's total
+  for (int w = 0; w < kCWarps; ++w) {
+    const uint32_t x = sh_warp[w];
+    if (w < warp) packed_in += x;
+    cta_total += x;
+  }
+  if (tid == 0) {
     for (uint32_t r = rank + 1; r < csize; ++r) ptx::dsmem_st_u32(ptx::map_rank(counts + rank, r), cta_total);
     counts[kMaxCluster] = cta_total;
   }
-  ptx::cluster_sync();   // last access to another CTA's shared memory
+  if (alone)
+    __syncthreads();
+  else
+    ptx::cluster_sync();   // last access to another CTA's shared memory
   const uint32_t before = (uint32_t)lane < rank ? counts[lane] : 0u;
   const uint32_t gt_before = warp_sum_u32(before >> 16), eq_before = warp_sum_u32(before & 0xffffu);
-  // Output position of this run: every greater value before it, plus the equal values before it
+  // Output position of a kept value: every greater value before it, plus the equal values before it
   // that are kept (the lowest-index need_eq copies of tau are kept). The CTA's kept rows take the
   // output positions [p0, p0 + n_kept); `kept` (the histogram space) lists them in order.
   const uint32_t p0 = gt_before + (eq_before < need_eq ? eq_before : need_eq);
@@ -374,74 +503,34 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
                           (eq_before < need_eq ? eq_before : need_eq);
   uint32_t* kept = work;
   const int kept_cap = round4(max(min(slice, kPoolChunk) + 2 * radius, kHistWords));   // the work space
-  const uint32_t e0 = eq_before + (packed_in & 0xffffu);
-  uint32_t pos = gt_before + (packed_in >> 16) + (e0 < need_eq ? e0 : need_eq);
-  uint32_t e = e0;
-  for (int j = a0; j < a1; ++j) {
-    const uint32_t u = pbits[j] & mask;
-    bool keep = u > tau;
-    if (u == tau) {
-      keep = e < need_eq;
-      ++e;
-    }
-    if (keep) {
+  uint32_t g_run = gt_before + (packed_in >> 16);      // greater values before this warp's next chunk
+  uint32_t e_run = eq_before + (packed_in & 0xffffu);  // equal values before it
+  for (int base = s0; base < s1; base += 32) {
+    const int j = base + lane;
+    const uint32_t u = j < s1 ? (pbits[j] & mask) : 0u;
+    const bool is_gt = j < s1 && u > tau, is_eq = j < s1 && u == tau;
+    const uint32_t gtb = __ballot_sync(0xffffffffu, is_gt), eqb = __ballot_sync(0xffffffffu, is_eq);
+    const uint32_t e_rank = e_run + __popc(eqb & lt_mask);
+    if (is_gt || (is_eq && e_rank < need_eq)) {
+      const uint32_t pos = g_run + __popc(gtb & lt_mask) + (e_rank < need_eq ? e_rank : need_eq);
       if ((int64_t)pos < k_sel) {
         idx[pos] = j0 + j;
-        if (pos - p0 < (uint32_t)kept_cap)
-          kept[pos - p0] = (uint32_t)(j0 + j);
-        else
-          report(g.dev_status, SNAPKV_ERR_INTERNAL);
+        if (pos - p0 < (uint32_t)kept_cap) kept[pos - p0] = (uint32_t)(j0 + j);
       }
-      ++pos;
     }
+    g_run += __popc(gtb);
+    e_run += __popc(eqb);
   }
   __syncthreads();
 
-  // Gather: this CTA's kept rows, then window rows rank, rank + csize, ... (16-byte pieces, four
-  // rows' worth of loads in flight per thread; the destinations are recomputed for the stores
-  // rather than held in registers across the loads, which keeps the kernel free of spills).
-  const int vpr = g.vpr;
-  const uint4* kin = g.k + bh * g.kv_stride * vpr;
-  const uint4* vin = g.v + bh * g.kv_stride * vpr;
-  uint4* kout = g.k_out + bh * g.cap * vpr;
-  uint4* vout = g.v_out + bh * g.cap * vpr;
-  const int n_win = (g.l_obs - (int)rank + (int)csize - 1) / (int)csize;   // window rows of this CTA
   // The kept rows land in [p0, p0 + n_kept) of the first k_sel cache rows, and every one of them
   // was listed above; an inconsistent count would be a library bug: reported, not followed.
   uint32_t n_rows = n_kept;
-  if ((int64_t)p0 + n_kept > k_sel || n_kept > (uint32_t)kept_cap) {
+  if ((int64_t)p0 + n_kept > k_sel) {
     if (tid == 0) report(g.dev_status, SNAPKV_ERR_INTERNAL);
     n_rows = 0;
   }
-  const int64_t items = ((int64_t)n_rows + n_win) * vpr;
-  constexpr int U = 4;
-  const int vsh = __ffs(vpr) - 1;   // 16-byte pieces per row: 8, 16 or 32
-  for (int64_t base = tid; base < items; base += (int64_t)U * kCThreads) {
-    uint4 kv[U], vv[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t it = base + (int64_t)u * kCThreads;
-      if (it < items) {
-        const int64_t row = it >> vsh;
-        const int c = (int)(it & (vpr - 1));
-        const int64_t src = row < (int64_t)n_rows ? (int64_t)kept[row]
-                                                  : l_prefix + (int64_t)rank + (row - n_rows) * csize;
-        kv[u] = ld_stream_v4(kin + src * vpr + c);
-        vv[u] = ld_stream_v4(vin + src * vpr + c);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t it = base + (int64_t)u * kCThreads;
-      if (it < items) {
-        const int64_t row = it >> vsh;
-        const int c = (int)(it & (vpr - 1));
-        const int64_t out = row < (int64_t)n_rows ? (int64_t)p0 + row : k_sel + (int64_t)rank + (row - n_rows) * csize;
-        kout[out * vpr + c] = kv[u];
-        vout[out * vpr + c] = vv[u];
-      }
-    }
-  }
+  gather_rows(g, bh, rank, csize, n_kept <= (uint32_t)kept_cap ? kept : nullptr, idx, p0, n_rows, l_prefix, k_sel);
   if (rank == 0 && tid == 0 && bh % g.heads == 0) g.len_out[bh / g.heads] = (int32_t)(k_sel + g.l_obs);
 }
 
@@ -465,13 +554,13 @@ cudaError_t launch_pool_topk(const CompressJob& job, bool* gathered) {
   } else if (job.n_var > 0 && !(job.l_prefix <= kClusterMaxPrefix && job.pool_kernel <= 1025)) {
     err = cudaErrorInvalidValue;   // a ragged batch takes the cluster kernel only
   } else if (job.l_prefix <= kClusterMaxPrefix && job.pool_kernel <= 1025) {
-    // CTAs per head. A head's select is latency-bound (a few radix passes, each ending in a cluster
-    // barrier), so a small batch spreads each head over up to 8 CTAs; a large batch fills the GPU
-    // with heads instead and keeps each on few CTAs, which saves the cross-CTA exchanges (256 heads
-    // of 16K keys: 8 CTAs per head 126 us, 4: 93 us, 2: 82 us, 1: 92 us per launch). The preferred
-    // size is the largest power of two with at most about four CTAs per SM in total, at least 2048
-    // keys per CTA, and at most kClusterMaxSlice keys per CTA.
-    const int64_t fill = (int64_t)4 * device_sm_count();
+    // CTAs per head. A head's select is latency-bound (a few radix passes, each ending in a barrier),
+    // so a small batch spreads each head over up to 8 CTAs of a cluster; once the heads alone give
+    // about two CTAs per SM, each head stays on one CTA (no cross-CTA exchange) and the GPU is filled
+    // with heads instead (256 heads of 16K keys: 8 CTAs per head 126 us, 2: 70 us, 1: 65 us per
+    // launch). The size is the largest power of two with at most about two CTAs per SM in total, at
+    // least 2048 keys per CTA, and at most kClusterMaxSlice keys per CTA.
+    const int64_t fill = (int64_t)2 * device_sm_count();
     int cl = 1;
     while (cl < kMaxCluster && (int64_t)(2 * cl) * bh <= fill) cl *= 2;
     const int by_keys = (int)((job.l_prefix + 2047) / 2048);
@@ -480,25 +569,6 @@ cudaError_t launch_pool_topk(const CompressJob& job, bool* gathered) {
     if (cl < need) cl = need;
     if (cl > kMaxCluster) cl = kMaxCluster;
     if (cl < 1) cl = 1;
-    const int slice = (int)((job.l_prefix + cl - 1) / cl);
-    const int work = (slice < kPoolChunk ? slice : kPoolChunk) + 2 * (job.pool_kernel / 2);
-    const size_t smem =
-        (size_t)(round4(slice) + round4(work > kHistWords ? work : kHistWords) + kSumWords + 32 + kMaxCluster + 1) *
-        sizeof(uint32_t);
-    err = cudaFuncSetAttribute(pool_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(bh * cl));
-    cfg.blockDim = dim3(kCThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = job.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     GatherArgs g;
     g.k = static_cast<const uint4*>(job.k);
     g.v = static_cast<const uint4*>(job.v);
@@ -523,8 +593,28 @@ cudaError_t launch_pool_topk(const CompressJob& job, bool* gathered) {
         if (g.var.k[b] < 1) return cudaErrorInvalidValue;   // a ragged launch keeps at least one row
       }
     }
-    err = cudaLaunchKernelEx(&cfg, pool_topk_cluster_kernel, (const float*)job.c, job.idx, job.l_prefix,
-                             job.pool_kernel / 2, job.k_sel, slice, g);
+    const int radius = job.pool_kernel / 2;
+    const int slice = (int)((job.l_prefix + cl - 1) / cl);
+    const int work = (slice < kPoolChunk ? slice : kPoolChunk) + 2 * radius;
+    const size_t smem =
+        (size_t)(round4(slice) + round4(work > kHistWords ? work : kHistWords) + kSumWords + 32 + kMaxCluster + 1) *
+        sizeof(uint32_t);
+    err = cudaFuncSetAttribute(pool_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(bh * cl));
+    cfg.blockDim = dim3(kCThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = job.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, pool_topk_cluster_kernel, (const float*)job.c, job.idx, job.l_prefix, radius,
+                             job.k_sel, slice, g);
     if (gathered) *gathered = err == cudaSuccess;
   } else {
     pool_topk_kernel<<<(unsigned)bh, kThreads, 0, job.stream>>>(job.c, job.p, job.idx, job.l_prefix,

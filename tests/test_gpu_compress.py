@@ -157,20 +157,41 @@ def test_prefill_32_layers_parity_coverage(dev):
     print(f"32-layer prefill: {len(jobs)} heads over {len(units)} layers, {excused} boundary-excused indices")
 
 
-@pytest.mark.parametrize("batch,l_prompt", [(16, 4096), (4, 8192), (2, 12000)])
-def test_large_batch_cluster_shapes(dev, batch, l_prompt):
-    """Batches that give the top-k kernel one, four and six CTAs per head (its cluster shrinks as the
-    heads alone fill the GPU), with the decode-shaped budget rule; every head against the oracle."""
+@pytest.mark.parametrize("batch,l_prompt,budget", [(16, 4096, 0), (4, 8192, 0), (2, 12000, 0), (10, 12000, 6000),
+                                                   (4, 16384, 12000)])
+def test_large_batch_top_k_shapes(dev, batch, l_prompt, budget):
+    """Batches that put the pooled top-k on one CTA per head (its own kernel, the boundary bin's values
+    in a candidate list), on clusters of two and four CTAs, and kept lists longer than the shared-memory
+    list a CTA holds (6000 kept rows on one CTA, about 6000 per CTA of a 2-CTA cluster), so that the
+    gather reads the kept positions back from the index output; every head against the oracle."""
     from kv_cache_compression_gb300 import snapkv
-    wl = synth.WORKLOADS[2].with_(batch=batch, l_prompt=l_prompt, layers=1)
+    wl = synth.WORKLOADS[2].with_(batch=batch, l_prompt=l_prompt, layers=1, budget=budget)
     q, k, v, _ = synth.device_inputs(wl, 5, 0, batch, l_prompt, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    res = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, ratio_p=wl.ratio_p, want_vote=True, dev_status=status)
+    res = snapkv.compress(q, k, v, pool_kernel=wl.pool_kernel, ratio_p=wl.ratio_p, budget=budget, want_vote=True,
+                          dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     jobs = _compress_jobs(wl, res, 5, 0, [(b, h) for b in range(batch) for h in range(wl.heads)], l_prompt)
     del q, k, v
     _pool_verdict(oracle_pool.run(oracle_pool.check_compress_job, jobs))
+
+
+def test_zero_queries_keep_the_first_k_at_large_batch(dev):
+    """q = 0 on a batch of 320 heads (one CTA per head): every pooled score is equal, the first digit's
+    bin holds the whole prefix (too many values for the candidate list), and ties go to the lower
+    index, so I = 0..k-1 exactly; likewise when k is larger than the CTA's shared-memory kept list."""
+    from kv_cache_compression_gb300 import snapkv
+    B, H, L, lo, d = 10, 32, 8000, 32, 128
+    k = torch.randn(B, H, L, d, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16).to(dev)
+    q = torch.zeros(B, H, lo, d, dtype=torch.bfloat16, device=dev)
+    for budget in (300, 5000):
+        res = snapkv.compress(q, k, k, pool_kernel=7, budget=budget)
+        torch.cuda.synchronize()
+        want = torch.arange(budget, dtype=torch.int32, device=dev).expand(B, H, budget)
+        assert torch.equal(res["idx"], want)
+        assert torch.equal(res["k_out"][:, :, :budget], k[:, :, :budget])
+        assert torch.equal(res["k_out"][:, :, budget:], k[:, :, L - lo:])
 
 
 def test_ragged_prompts_sampled(dev):

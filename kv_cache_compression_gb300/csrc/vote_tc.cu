@@ -44,6 +44,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <cstdlib>
 
 #include "sm100_ptx.cuh"
 #include "snapkv_common.cuh"
@@ -89,6 +90,7 @@ struct TcArgs {
   int group;         // query heads per KV head: head h reads the keys of KV head h / group
   int resident;      // 1: one item per key chunk, logits stay in TMEM from statistics to vote
   float scale_log2;
+  long long wait_limit;   // SM cycles after which a bounded wait gives up (kWaitLimit unless testing)
   double* zsum;      // [BH][l_obs]: Z_i = sum_j 2^(s'_ij) over the head's visible keys (fp64)
   uint32_t* cnt;     // [BH] A items whose contribution to zsum is complete
   float* c_out;      // [BH][c_stride]
@@ -293,7 +295,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         if (p >= a.n_queue || *c.abort) break;
         const Item it = queue_item<VAR>(a, p);
         const int qb = n & 1;
-        if (!ptx::mbar_wait(&c.q_empty[qb], ((n >> 1) & 1) ^ 1, c.abort, kWaitLimit)) {
+        if (!ptx::mbar_wait(&c.q_empty[qb], ((n >> 1) & 1) ^ 1, c.abort, a.wait_limit)) {
           fail(c, a.dev_status);
           break;
         }
@@ -313,7 +315,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         for (int t = 0; t < tiles; ++t, ++g) {
           const int stage = g % Lay::STAGES;
           const uint32_t round = g / Lay::STAGES;
-          if (!ptx::mbar_wait(&c.empty[stage], (round & 1) ^ 1, c.abort, kWaitLimit)) {
+          if (!ptx::mbar_wait(&c.empty[stage], (round & 1) ^ 1, c.abort, a.wait_limit)) {
             fail(c, a.dev_status);
             ok = false;
             break;
@@ -347,8 +349,8 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         if (p >= a.n_queue || *c.abort) break;
         const Item it = queue_item<VAR>(a, p);
         const int slot = n % kSlots, use = n / kSlots, qb = n & 1;
-        if (!ptx::mbar_wait(&c.tmem_empty[slot], (use & 1) ^ 1, c.abort, kWaitLimit) ||
-            !ptx::mbar_wait(&c.q_full[qb], (n >> 1) & 1, c.abort, kWaitLimit)) {
+        if (!ptx::mbar_wait(&c.tmem_empty[slot], (use & 1) ^ 1, c.abort, a.wait_limit) ||
+            !ptx::mbar_wait(&c.q_full[qb], (n >> 1) & 1, c.abort, a.wait_limit)) {
           fail(c, a.dev_status);
           break;
         }
@@ -360,7 +362,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
           if (t < tiles) {
             const int stage = g % Lay::STAGES;
             const uint32_t round = g / Lay::STAGES;
-            if (!ptx::mbar_wait(&c.full[stage], round & 1, c.abort, kWaitLimit)) {
+            if (!ptx::mbar_wait(&c.full[stage], round & 1, c.abort, a.wait_limit)) {
               fail(c, a.dev_status);
               ok = false;
               break;
@@ -435,7 +437,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     // every barrier.
     auto wait_tiles = [&](int slot, int use) {
       for (int t = 0; t < TI; ++t)
-        if (!ptx::mbar_wait(&c.tile_full[slot * TI + t], use & 1, c.abort, kWaitLimit)) fail(c, a.dev_status);
+        if (!ptx::mbar_wait(&c.tile_full[slot * TI + t], use & 1, c.abort, a.wait_limit)) fail(c, a.dev_status);
       ptx::tc_fence_after();
     };
 
@@ -632,7 +634,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         if (ptx::ld_acquire_u32(a.cnt + it.head) < need) {
           const long long t0 = clock64();
           while (ptx::ld_acquire_u32(a.cnt + it.head) < need) {
-            if (*c.abort || clock64() - t0 > kWaitLimit) {
+            if (*c.abort || clock64() - t0 > a.wait_limit) {
               fail(c, a.dev_status);
               break;
             }
@@ -773,6 +775,14 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   if (delta < 1) delta = 1;
   a.delta = (int)(delta < bh ? delta : bh);
   a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)job.head_dim));
+  // Testing knob: SNAPKV_WAIT_LIMIT_CYCLES (a positive count of SM cycles) shortens every bounded
+  // wait of this kernel, so that a test can make one run out and check the timeout report; unset, the
+  // waits give up after ~2 s only.
+  a.wait_limit = kWaitLimit;
+  if (const char* env = getenv("SNAPKV_WAIT_LIMIT_CYCLES")) {
+    const long long v = strtoll(env, nullptr, 10);
+    if (v > 0) a.wait_limit = v;
+  }
   a.zsum = job.tc_zsum;
   a.cnt = job.tc_cnt;
   a.c_out = group > 1 ? job.c_q : job.c;

@@ -7,7 +7,7 @@ import torch
 
 import synth
 from oracle import snapkv_oracle as orc
-from tests.parity import check_compress_head, check_decode, to_numpy_f32
+from tests.parity import assert_canary, canary_like, check_compress_head, check_decode, to_numpy_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -49,10 +49,17 @@ def test_varlen_ratio_rule_bf16(dev, algo):
     wl = synth.WORKLOADS[1].with_(heads=6, plants=16)
     lengths = [4096, 2500, 5001, 417]
     q, k, v = synth.device_inputs_padded(wl, 0, 0, lengths, dev)
+    k_max = orc.kept_slots(max(lengths) - wl.l_obs, ratio_p=0.1)
+    cap = k_max + wl.l_obs + 2   # every sequence's rows past its own k_b + L_obs are a canary guard band
+    k_out = canary_like((len(lengths), wl.heads, cap, wl.head_dim), torch.bfloat16, dev)
+    v_out = canary_like((len(lengths), wl.heads, cap, wl.head_dim), torch.bfloat16, dev)
     res = snapkv.compress_varlen(q, k, v, lengths, pool_kernel=wl.pool_kernel, ratio_p=0.1, algo=algo,
-                                 want_vote=True)
+                                 want_vote=True, k_out=k_out, v_out=v_out)
     torch.cuda.synchronize()
     assert len(set(res["ks"])) == len(lengths)               # truly ragged k
+    for b, kb in enumerate(res["ks"]):
+        assert_canary(k_out[b, :, kb + wl.l_obs:], f"seq {b}: k_out rows past k_b + L_obs")
+        assert_canary(v_out[b, :, kb + wl.l_obs:], f"seq {b}: v_out rows past k_b + L_obs")
     _check(res, wl, lengths, range(wl.heads), ratio_p=0.1, budget=0)
 
 

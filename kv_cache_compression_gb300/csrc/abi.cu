@@ -6,6 +6,8 @@
 
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "snapkv_common.cuh"
 #include "snapkv_internal.h"
 
@@ -20,6 +22,16 @@ constexpr int kMaxObs = 128;
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// An NVTX range around an entry point's host work (validation and enqueueing), so that a profiler's
+// timeline shows which library call enqueued which kernels; without a tool attached it costs a few
+// nanoseconds.
+struct HostRange {
+  explicit HostRange(const char* name) { nvtxRangePushA(name); }
+  ~HostRange() { nvtxRangePop(); }
+  HostRange(const HostRange&) = delete;
+  HostRange& operator=(const HostRange&) = delete;
+};
 
 bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
   const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
@@ -272,6 +284,7 @@ snapkv_status snapkv_compress_profiled(const snapkv_compress_params* params, con
                                        int32_t* idx_out, float* vote_out, void* workspace, size_t workspace_bytes,
                                        int32_t* dev_status, snapkv_stream_t stream, void* const* stage_events,
                                        int32_t n_events) {
+  HostRange nvtx_range("snapkv_compress");
   if (!params) return SNAPKV_ERR_INVALID_ARG;
   return compress_impl(params, params->heads, q_obs, k, v, k_out, v_out, cap, len_out, idx_out, vote_out, workspace,
                        workspace_bytes, dev_status, stream, stage_events, n_events);
@@ -281,6 +294,7 @@ snapkv_status snapkv_compress_gqa(const snapkv_compress_params* params, int32_t 
                                   const void* k, const void* v, void* k_out, void* v_out, int64_t cap,
                                   int32_t* len_out, int32_t* idx_out, float* vote_out, void* workspace,
                                   size_t workspace_bytes, int32_t* dev_status, snapkv_stream_t stream) {
+  HostRange nvtx_range("snapkv_compress_gqa");
   return compress_impl(params, q_heads, q_obs, k, v, k_out, v_out, cap, len_out, idx_out, vote_out, workspace,
                        workspace_bytes, dev_status, stream, nullptr, 0);
 }
@@ -310,6 +324,7 @@ snapkv_status snapkv_compress_varlen(const snapkv_compress_params* params, const
                                      int64_t cap, int32_t* len_out, int32_t* idx_out, float* vote_out,
                                      void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                      snapkv_stream_t stream) {
+  HostRange nvtx_range("snapkv_compress_varlen");
   int64_t lp_max = 0, k_max = 0;
   int rows = 0;
   if (!params || !l_prompts) return SNAPKV_ERR_INVALID_ARG;
@@ -468,6 +483,7 @@ snapkv_status snapkv_compress(const snapkv_compress_params* params, const void* 
 snapkv_status snapkv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int64_t cap,
                             int32_t* len, int32_t batch, int32_t heads, int32_t head_dim, int32_t dtype,
                             int32_t* dev_status, snapkv_stream_t stream) {
+  HostRange nvtx_range("snapkv_append");
   if (!k_new || !v_new || !k_cache || !v_cache || !len) return SNAPKV_ERR_INVALID_ARG;
   if (batch < 1 || heads < 1 || head_dim < 1 || cap < 1 || cap > kMaxPrompt) return SNAPKV_ERR_INVALID_ARG;
   if (dtype != SNAPKV_F32 && dtype != SNAPKV_BF16) return SNAPKV_ERR_INVALID_ARG;
@@ -492,6 +508,7 @@ snapkv_status snapkv_decode_attend(const void* q, const void* k_cache, const voi
                                    const int32_t* len, void* out, int32_t batch, int32_t heads, int32_t head_dim,
                                    int32_t dtype, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                    snapkv_stream_t stream) {
+  HostRange nvtx_range("snapkv_decode_attend");
   if (!q || !k_cache || !v_cache || !len || !out) return SNAPKV_ERR_INVALID_ARG;
   if (batch < 1 || heads < 1 || head_dim < 1 || cap < 1 || cap > kMaxPrompt) return SNAPKV_ERR_INVALID_ARG;
   if (dtype != SNAPKV_F32 && dtype != SNAPKV_BF16) return SNAPKV_ERR_INVALID_ARG;
@@ -529,6 +546,7 @@ snapkv_status snapkv_append_decode_attend(const void* q, const void* k_new, cons
                                           void* out, int32_t batch, int32_t heads, int32_t head_dim, int32_t dtype,
                                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                           snapkv_stream_t stream) {
+  HostRange nvtx_range("snapkv_append_decode_attend");
   if (!q || !k_new || !v_new || !k_cache || !v_cache || !len_in || !len_out || !out) return SNAPKV_ERR_INVALID_ARG;
   if (batch < 1 || heads < 1 || head_dim < 1 || cap < 1 || cap > kMaxPrompt) return SNAPKV_ERR_INVALID_ARG;
   if (dtype != SNAPKV_F32 && dtype != SNAPKV_BF16) return SNAPKV_ERR_INVALID_ARG;
@@ -580,6 +598,7 @@ snapkv_status snapkv_decode_attend_noalloc(const void* q, const void* k_cache, c
                                            const int32_t* len, void* out, int32_t batch, int32_t heads,
                                            int32_t head_dim, int32_t dtype, int32_t* dev_status,
                                            snapkv_stream_t stream) {
+  HostRange nvtx_range("snapkv_decode_attend_noalloc");
   if (!q || !k_cache || !v_cache || !len || !out) return SNAPKV_ERR_INVALID_ARG;
   if (batch < 1 || heads < 1 || head_dim < 1 || cap < 1 || cap > kMaxPrompt) return SNAPKV_ERR_INVALID_ARG;
   if (dtype != SNAPKV_F32 && dtype != SNAPKV_BF16) return SNAPKV_ERR_INVALID_ARG;
@@ -618,6 +637,7 @@ snapkv_status snapkv_hit_rate(const void* q, const void* k_cache, int64_t cap, c
                               const int32_t* idx, int64_t k, int32_t batch, int32_t heads, int32_t head_dim,
                               int32_t dtype, double theta, int32_t* hits, int32_t* total, int32_t* dev_status,
                               snapkv_stream_t stream) {
+  HostRange nvtx_range("snapkv_hit_rate");
   if (!q || !k_cache || !len || !hits || !total || (k > 0 && !idx)) return SNAPKV_ERR_INVALID_ARG;
   if (batch < 1 || heads < 1 || cap < 1 || cap > kMaxPrompt || k < 0) return SNAPKV_ERR_INVALID_ARG;
   if ((int64_t)batch * heads > 2147483647LL) return SNAPKV_ERR_INVALID_ARG;

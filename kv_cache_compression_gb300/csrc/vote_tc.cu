@@ -172,14 +172,16 @@ struct TcLayout {
   // flight already keep HBM busy, and a deeper ring only lengthens the memory queues that the
   // epilogue's reductions, counter updates and vote stores wait in (8 stages: 39.3 us per launch
   // of the 16K-key layer, 3 stages: 34.6 us).
-  static constexpr int FIXED = 2 * Q_BYTES + 2 * 4 * N * 4 + 2 * N * 4 + 8 * (2 * 8 + 4 + 4 * 16 + 4 + 1) + 64 + 1024;
+  static constexpr int FIXED =
+      2 * Q_BYTES + 2 * 4 * N * 4 + 2 * N * 4 + kSlots * N * 4 + 8 * (2 * 8 + 4 + 4 * 16 + 4 + 1) + 64 + 1024;
   static constexpr int STAGES_FIT = (232448 - FIXED) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT < 3 ? STAGES_FIT : 3;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_Q = OFF_K + STAGES * STAGE_BYTES;
   static constexpr int OFF_RED = OFF_Q + 2 * Q_BYTES;        // [2 groups][4 warps][N] floats
   static constexpr int OFF_ROW = OFF_RED + 2 * 4 * N * 4;    // [2 groups][N] floats: per-row constants
-  static constexpr int OFF_BAR = OFF_ROW + 2 * N * 4;
+  static constexpr int OFF_SMAX = OFF_ROW + 2 * N * 4;      // [kSlots][N] floats: an item's row maxima
+  static constexpr int OFF_BAR = OFF_SMAX + kSlots * N * 4;
   static constexpr int NBAR = 2 * STAGES + 4 + kSlots * TI + kSlots + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // + slack for 1024-byte alignment; at least 120 KB so that no two CTAs share an SM (each one
@@ -248,6 +250,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
   c.abort = reinterpret_cast<volatile int*>(c.misc + 1);
   float* red = reinterpret_cast<float*>(base + Lay::OFF_RED);
   float* rowc = reinterpret_cast<float*>(base + Lay::OFF_ROW);
+  float* slot_max = reinterpret_cast<float*>(base + Lay::OFF_SMAX);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -424,6 +427,11 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       for (int h = 0; h < R; h += 16) ptx::tmem_ld16(tmem_base + lane_addr + col + h, acc + h);
       ptx::tmem_wait_ld();
     };
+    auto store_rows = [&](uint32_t col, const float* val) {
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < R; h += 16) ptx::tmem_st16(tmem_base + lane_addr + col + h, val + h);
+    };
     // Per-warp row results after a butterfly: lane l holds row l (R == 32) or l/2 (R == 16).
     auto stash_rows = [&](float* v, int r0) {
       if constexpr (R == 32) {
@@ -482,6 +490,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
           for (int w = 1; w < 4; ++w) mx = fmaxf(mx, gred[w * N + r0 + gtid]);
           growc[r0 + gtid] = mx * a.scale_log2;       // log2-domain row maximum (or -inf)
+          slot_max[slot * N + r0 + gtid] = mx * a.scale_log2;   // kept for the item's vote
         }
         ptx::named_barrier(bar_id, 128);
         float mrow[R];
@@ -491,11 +500,15 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         for (int i = 0; i < R; ++i) v[i] = 0.f;
         for (int t = 0; t < tiles; ++t) {
           float acc[R];
-          load_rows((uint32_t)(slot * TI * N + t * N + r0), acc);
+          const uint32_t col = (uint32_t)(slot * TI * N + t * N + r0);
+          load_rows(col, acc);
           const int64_t tkey0 = item_key0 + t * kTileKeys;
           if (tkey0 + kTileKeys <= l_prefix) {
 #pragma unroll
-            for (int i = 0; i < R; ++i) v[i] += ex2(fmaf(acc[i], a.scale_log2, -mrow[i]));
+            for (int i = 0; i < R; ++i) {
+              acc[i] = ex2(fmaf(acc[i], a.scale_log2, -mrow[i]));
+              v[i] += acc[i];
+            }
           } else {
             const int64_t key = tkey0 + key_in_tile;
 #pragma unroll
@@ -503,10 +516,14 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
               const int row = r0 + i;
               const bool vis = row < a.l_obs && key < l_prompt &&
                                (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + row : key <= lim);
-              if (vis) v[i] += ex2(fmaf(acc[i], a.scale_log2, -mrow[i]));
+              acc[i] = vis ? ex2(fmaf(acc[i], a.scale_log2, -mrow[i])) : 0.f;
+              v[i] += acc[i];
             }
           }
+          // A resident item's vote reads these exponentials back: 2^(s' - M_item) in place of s'.
+          if (a.resident) store_rows(col, acc);
         }
+        if (a.resident) ptx::tmem_wait_st();
         const bool last_read = !a.resident && r0 + R >= N;   // resident items keep the slot
         if (last_read) ptx::tc_fence_before();
         tc::butterfly_sum<R, 16>(v, lane);
@@ -545,15 +562,24 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       const int64_t l_prompt = prompt_of<VAR>(a, it);
       const int64_t l_prefix = VAR ? l_prompt - a.l_obs : a.l_prefix;
       const int64_t lim = a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? l_prefix : l_prefix - 1;
-      // Folds the visible logits of rows rb .. rb + R - 1 of tile t into v (max or sum of 2^(s'-M)).
+      // Folds the visible logits of rows rb .. rb + R - 1 of tile t into v (max, or sum of 2^(s'-M));
+      // the sum also writes each 2^(s'-M) (0 where not visible) back over its logit for the vote of
+      // a resident item.
       auto fold = [&](int t, int rb, float* v, bool sum) {
         float acc[R];
-        load_rows((uint32_t)(slot * TI * N + t * N + rb), acc);
+        const uint32_t col = (uint32_t)(slot * TI * N + t * N + rb);
+        load_rows(col, acc);
         const int64_t tkey0 = item_key0 + t * kTileKeys;
         if (tkey0 + kTileKeys <= l_prefix) {
 #pragma unroll
-          for (int i = 0; i < R; ++i)
-            v[i] = sum ? v[i] + ex2(fmaf(acc[i], a.scale_log2, -growc[rb + i])) : fmaxf(v[i], acc[i]);
+          for (int i = 0; i < R; ++i) {
+            if (sum) {
+              acc[i] = ex2(fmaf(acc[i], a.scale_log2, -growc[rb + i]));
+              v[i] += acc[i];
+            } else {
+              v[i] = fmaxf(v[i], acc[i]);
+            }
+          }
         } else {
           const int64_t key = tkey0 + key_in_tile;
 #pragma unroll
@@ -561,9 +587,15 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
             const int row = rb + i;
             const bool vis = row < a.l_obs && key < l_prompt &&
                              (a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? key <= lim + row : key <= lim);
-            if (vis) v[i] = sum ? v[i] + ex2(fmaf(acc[i], a.scale_log2, -growc[rb + i])) : fmaxf(v[i], acc[i]);
+            if (sum) {
+              acc[i] = vis ? ex2(fmaf(acc[i], a.scale_log2, -growc[rb + i])) : 0.f;
+              v[i] += acc[i];
+            } else if (vis) {
+              v[i] = fmaxf(v[i], acc[i]);
+            }
           }
         }
+        if (sum && a.resident) store_rows(col, acc);
       };
       wait_tiles(slot, n / kSlots);
 #pragma unroll 1
@@ -587,6 +619,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
           for (int w = 1; w < 4; ++w) mx = fmaxf(mx, gred[w * N + r0 + gtid]);
           growc[r0 + gtid] = mx * a.scale_log2;       // log2-domain row maximum (or -inf)
+          slot_max[slot * N + r0 + gtid] = mx * a.scale_log2;   // kept for the item's vote
         }
         ptx::named_barrier(bar_id, 128);
         const bool last_read = !a.resident && r0 + 2 * R >= N;   // resident items keep the slot
@@ -597,6 +630,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
           for (int i = 0; i < R; ++i) v[i] = 0.f;
           for (int t = 0; t < tiles; ++t) fold(t, rb, v, true);
+          if (a.resident) ptx::tmem_wait_st();
           if (last_read && h == 1) ptx::tc_fence_before();
           tc::butterfly_sum<R, 16>(v, lane);
           stash_rows(v, rb);
@@ -652,24 +686,43 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
           const float mant = __uint_as_float(0x3F800000u | (uint32_t)((zb >> 29) & 0x7FFFFF));
           cv = (zb & 0x7FF0000000000000LL) ? (float)e + log2f(mant) : -INFINITY;
         }
-        growc[gtid] = cv;
+        // A resident item's slot holds 2^(s' - M_i) (M_i its row maximum): the weight is that times
+        // f_i = 2^(M_i - log2 Z_i) <= 1, and 0 for rows past L_obs. Otherwise the slot holds the
+        // logits and the row constant is log2 Z_i itself.
+        growc[gtid] = a.resident ? (gtid < a.l_obs ? ex2(slot_max[slot * N + gtid] - cv) : 0.f) : cv;
       }
       wait_tiles(slot, n / kSlots);
       ptx::named_barrier(bar_id, 128);
       float cr[N];
 #pragma unroll
       for (int i = 0; i < N; ++i) cr[i] = growc[i];
-      for (int t = 0; t < tiles; ++t) {
-        const int64_t key = item_key0 + t * kTileKeys + key_in_tile;
-        float csum = 0.f;
+      const int64_t vote_end = VAR ? prompt_of<VAR>(a, it) - a.l_obs : a.l_prefix;   // prefix keys only
+      if (a.resident) {
+        for (int t = 0; t < tiles; ++t) {
+          const int64_t key = item_key0 + t * kTileKeys + key_in_tile;
+          float csum = 0.f;
 #pragma unroll
-        for (int r0 = 0; r0 < N; r0 += R) {
-          float acc[R];
-          load_rows((uint32_t)(slot * TI * N + t * N + r0), acc);
+          for (int r0 = 0; r0 < N; r0 += R) {
+            float acc[R];
+            load_rows((uint32_t)(slot * TI * N + t * N + r0), acc);
 #pragma unroll
-          for (int i = 0; i < R; ++i) csum += ex2(fmaf(acc[i], a.scale_log2, -cr[r0 + i]));
+            for (int i = 0; i < R; ++i) csum = fmaf(acc[i], cr[r0 + i], csum);
+          }
+          if (key < vote_end) a.c_out[(int64_t)it.head * a.c_stride + key] = csum;
         }
-        if (key < (VAR ? prompt_of<VAR>(a, it) - a.l_obs : a.l_prefix)) a.c_out[(int64_t)it.head * a.c_stride + key] = csum;
+      } else {
+        for (int t = 0; t < tiles; ++t) {
+          const int64_t key = item_key0 + t * kTileKeys + key_in_tile;
+          float csum = 0.f;
+#pragma unroll
+          for (int r0 = 0; r0 < N; r0 += R) {
+            float acc[R];
+            load_rows((uint32_t)(slot * TI * N + t * N + r0), acc);
+#pragma unroll
+            for (int i = 0; i < R; ++i) csum += ex2(fmaf(acc[i], a.scale_log2, -cr[r0 + i]));
+          }
+          if (key < vote_end) a.c_out[(int64_t)it.head * a.c_stride + key] = csum;
+        }
       }
       ptx::tc_fence_before();
       ptx::named_barrier(bar_id, 128);

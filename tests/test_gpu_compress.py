@@ -158,12 +158,13 @@ def test_prefill_32_layers_parity_coverage(dev):
 
 
 @pytest.mark.parametrize("batch,l_prompt,budget", [(16, 4096, 0), (4, 8192, 0), (2, 12000, 0), (10, 12000, 6000),
-                                                   (4, 16384, 12000)])
+                                                   (4, 16384, 12000), (12, 3000, 2968)])
 def test_large_batch_top_k_shapes(dev, batch, l_prompt, budget):
     """Batches that put the pooled top-k on one CTA per head (its own kernel, the boundary bin's values
     in a candidate list), on clusters of two and four CTAs, and kept lists longer than the shared-memory
     list a CTA holds (6000 kept rows on one CTA, about 6000 per CTA of a 2-CTA cluster), so that the
-    gather reads the kept positions back from the index output; every head against the oracle."""
+    gather reads the kept positions back from the index output; and a batch keeping its whole prefix;
+    every head against the oracle."""
     from kv_cache_compression_gb300 import snapkv
     wl = synth.WORKLOADS[2].with_(batch=batch, l_prompt=l_prompt, layers=1, budget=budget)
     q, k, v, _ = synth.device_inputs(wl, 5, 0, batch, l_prompt, dev)

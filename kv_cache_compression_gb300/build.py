@@ -1,4 +1,8 @@
-"""Build libsnapkv.so in-tree for sm_103a with nvcc (one -gencode, translation units in parallel)."""
+"""Build libsnapkv.so in-tree for sm_103a with nvcc (one -gencode, translation units in parallel).
+
+build(checked=True) makes libsnapkv_checked.so instead: the same kernels compiled with
+-DSNAPKV_CHECKED, where every global index a kernel computes is checked before the access and a
+violation is reported as SNAPKV_ERR_INTERNAL (the tests run part of the parity suite on it)."""
 from __future__ import annotations
 
 import os
@@ -16,8 +20,8 @@ FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", 
          "--expt-relaxed-constexpr"]
 
 
-def lib_path() -> str:
-    return os.path.join(_HERE, "libsnapkv.so")
+def lib_path(checked: bool = False) -> str:
+    return os.path.join(_HERE, "libsnapkv_checked.so" if checked else "libsnapkv.so")
 
 
 def nvcc() -> str:
@@ -41,18 +45,21 @@ def _stale(out, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile every kernel file and link libsnapkv.so next to this package."""
-    os.makedirs(_BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, checked: bool = False) -> str:
+    """Compile every kernel file and link libsnapkv.so (or the bounds-checked libsnapkv_checked.so)
+    next to this package."""
+    build_dir = _BUILD + ("_checked" if checked else "")
+    extra = ["-DSNAPKV_CHECKED"] if checked else []
+    os.makedirs(build_dir, exist_ok=True)
     header_deps = [os.path.join(_CSRC, h) for h in HEADERS] + [
         os.path.join(os.path.dirname(_HERE), "include", "snapkv.h")]
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(_CSRC, src)
-        o = os.path.join(_BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + header_deps):
-            cmd = [nvcc(), *ARCH, *FLAGS, "-c", s, "-o", o]
+            cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", s, "-o", o]
             if verbose_ptxas:
                 cmd += ["-Xptxas", "-v"]
             jobs.append(cmd)
@@ -60,7 +67,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if jobs:
         with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             logs = list(ex.map(_run, jobs))
-    out = lib_path()
+    out = lib_path(checked)
     if force or jobs or _stale(out, objs):
         tmp = out + ".tmp"
         _run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs])

@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecArgs a) {
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int r = rb + u * GROUPS;
-      if (r < r1) {
+      if (r < r1 && in_bounds(r >= 0 && r < a.cap, a.dev_status)) {
         kr[u] = ld_stream_v4(kc + (int64_t)r * D);
         vr[u] = ld_stream_v4(vc + (int64_t)r * D);
       } else {
@@ -317,10 +317,15 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(DecArgs a) {
   auto issue = [&](int c) {
     const int buf = c % kClBufs;
     const int cr0 = r0 + c * CH;
-    const uint32_t bytes = (uint32_t)(min(CH, r1 - cr0) * ROW_BYTES);
+    const int rows = min(CH, r1 - cr0);
+    // (a chunk that fails the check copies nothing, so its barrier still completes)
+    const bool ok = in_bounds(cr0 >= 0 && rows > 0 && cr0 + rows <= cap, a.dev_status);
+    const uint32_t bytes = ok ? (uint32_t)(rows * ROW_BYTES) : 0u;
     ptx::mbar_arrive_expect_tx(&bar[buf], 2 * bytes);
-    ptx::bulk_load(dsm + (2 * buf) * kClChunkBytes, kc + (int64_t)cr0 * D, bytes, &bar[buf]);
-    ptx::bulk_load(dsm + (2 * buf + 1) * kClChunkBytes, vc + (int64_t)cr0 * D, bytes, &bar[buf]);
+    if (ok) {
+      ptx::bulk_load(dsm + (2 * buf) * kClChunkBytes, kc + (int64_t)cr0 * D, bytes, &bar[buf]);
+      ptx::bulk_load(dsm + (2 * buf + 1) * kClChunkBytes, vc + (int64_t)cr0 * D, bytes, &bar[buf]);
+    }
   };
   if (tid == 0) {
     for (int i = 0; i < kClBufs; ++i) ptx::mbar_init(&bar[i], 1);

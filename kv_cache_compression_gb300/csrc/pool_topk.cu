@@ -351,8 +351,10 @@ __device__ __forceinline__ void gather_rows(const GatherArgs& g, int64_t bh, uin
           src = kept ? (int64_t)kept[row] : (int64_t)__ldcg(idx + p0 + row);
         else
           src = l_prefix + (int64_t)rank + (row - n_rows) * csize;
-        kv[u] = ld_stream_v4(kin + src * vpr + c);
-        vv[u] = ld_stream_v4(vin + src * vpr + c);
+        if (in_bounds(src >= 0 && src < g.kv_stride, g.dev_status)) {
+          kv[u] = ld_stream_v4(kin + src * vpr + c);
+          vv[u] = ld_stream_v4(vin + src * vpr + c);
+        }
       }
     }
 #pragma unroll
@@ -362,8 +364,10 @@ __device__ __forceinline__ void gather_rows(const GatherArgs& g, int64_t bh, uin
         const int64_t row = it >> vsh;
         const int c = (int)(it & (vpr - 1));
         const int64_t out = row < (int64_t)n_rows ? (int64_t)p0 + row : k_sel + (int64_t)rank + (row - n_rows) * csize;
-        kout[out * vpr + c] = kv[u];
-        vout[out * vpr + c] = vv[u];
+        if (in_bounds(out >= 0 && out < g.cap, g.dev_status)) {
+          kout[out * vpr + c] = kv[u];
+          vout[out * vpr + c] = vv[u];
+        }
       }
     }
   }

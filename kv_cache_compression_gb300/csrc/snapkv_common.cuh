@@ -35,6 +35,20 @@ __device__ __forceinline__ void report(int32_t* dev_status, int32_t bits) {
   if (dev_status) atomicOr(dev_status, bits);
 }
 
+// Bounds-checked build (compiled with -DSNAPKV_CHECKED): the global indices a kernel computes from
+// data or from its own bookkeeping are checked before the access; a violation is reported as
+// SNAPKV_ERR_INTERNAL (a library bug) and the access is skipped. The regular build compiles every
+// check away (the index arithmetic is correct by construction there, and the tests run the checked
+// build to show it).
+#ifdef SNAPKV_CHECKED
+__device__ __forceinline__ bool in_bounds(bool ok, int32_t* dev_status) {
+  if (!ok) report(dev_status, SNAPKV_ERR_INTERNAL);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(bool, int32_t*) { return true; }
+#endif
+
 // Element type traits: 16-byte vectors of 8 bf16 or 4 fp32, widened to fp32.
 template <typename T> struct Elem;
 template <> struct Elem<float> {

@@ -29,6 +29,7 @@ struct VoteParams {
   int64_t l_prompt, l_prefix, kv_stride;
   int l_obs, rows, scope, chunk, n_chunk_all;   // rows: window-query rows per head
   float scale_log2;     // log2(e) / sqrt(d)
+  int32_t* dev_status;  // the bounds-checked build reports here
 };
 
 template <int D, int QG>
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) vote_simt_kernel(VoteParams a, int p
         float c = red[j];
 #pragma unroll
         for (int q = 1; q < kGroups; ++q) c += red[q * kTile + j];
-        a.c_out[bh * a.l_prefix + col] = c;
+        if (in_bounds(col >= 0 && col < a.l_prefix, a.dev_status)) a.c_out[bh * a.l_prefix + col] = c;
       }
     }
   }
@@ -240,6 +241,7 @@ cudaError_t launch_vote_simt(const CompressJob& job) {
   a.l_prefix = job.l_prefix;
   a.l_obs = job.l_obs;
   a.rows = job.q_rows;
+  a.dev_status = job.dev_status;
   a.scope = job.scope;
   a.chunk = job.vote_chunk;
   a.n_chunk_all = job.n_chunk_all;

@@ -543,7 +543,8 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
             const uint32_t fb = __float_as_uint(zz * ex2(mx - fl));
             const long long e = (long long)fminf(fmaxf(fl, -1000.f), 1000.f) + (long long)((fb >> 23) & 0xFF) - 127;
             const long long db = ((e + 1023) << 52) | ((long long)(fb & 0x7FFFFF) << 29);
-            ptx::red_add_f64(a.zsum + (int64_t)it.head * a.l_obs + r0 + gtid, __longlong_as_double(db));
+            if (in_bounds(it.head < a.bh_total && r0 + gtid < a.l_obs, a.dev_status))
+              ptx::red_add_f64(a.zsum + (int64_t)it.head * a.l_obs + r0 + gtid, __longlong_as_double(db));
           }
         }
         ptx::named_barrier(bar_id, 128);
@@ -648,7 +649,8 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
             const uint32_t fb = __float_as_uint(zz * ex2(mx - fl));
             const long long e = (long long)fminf(fmaxf(fl, -1000.f), 1000.f) + (long long)((fb >> 23) & 0xFF) - 127;
             const long long db = ((e + 1023) << 52) | ((long long)(fb & 0x7FFFFF) << 29);
-            ptx::red_add_f64(a.zsum + (int64_t)it.head * a.l_obs + r0 + gtid, __longlong_as_double(db));
+            if (in_bounds(it.head < a.bh_total && r0 + gtid < a.l_obs, a.dev_status))
+              ptx::red_add_f64(a.zsum + (int64_t)it.head * a.l_obs + r0 + gtid, __longlong_as_double(db));
           }
         }
         ptx::named_barrier(bar_id, 128);
@@ -708,7 +710,8 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
             for (int i = 0; i < R; ++i) csum = fmaf(acc[i], cr[r0 + i], csum);
           }
-          if (key < vote_end) a.c_out[(int64_t)it.head * a.c_stride + key] = csum;
+          if (key < vote_end && in_bounds(it.head < a.bh_total && key < a.c_stride, a.dev_status))
+            a.c_out[(int64_t)it.head * a.c_stride + key] = csum;
         }
       } else {
         for (int t = 0; t < tiles; ++t) {
@@ -721,7 +724,8 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 #pragma unroll
             for (int i = 0; i < R; ++i) csum += ex2(fmaf(acc[i], a.scale_log2, -cr[r0 + i]));
           }
-          if (key < vote_end) a.c_out[(int64_t)it.head * a.c_stride + key] = csum;
+          if (key < vote_end && in_bounds(it.head < a.bh_total && key < a.c_stride, a.dev_status))
+            a.c_out[(int64_t)it.head * a.c_stride + key] = csum;
         }
       }
       ptx::tc_fence_before();

@@ -16,7 +16,8 @@ import re
 from typing import Optional
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "libsnapkv.so")
+# SNAPKV_CHECKED=1 selects the bounds-checked build (kv_cache_compression_gb300.build.build(checked=True)).
+_LIB_PATH = os.path.join(_HERE, "libsnapkv_checked.so" if os.environ.get("SNAPKV_CHECKED") == "1" else "libsnapkv.so")
 _HEADER = os.path.join(os.path.dirname(_HERE), "include", "snapkv.h")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_INTERNAL = (

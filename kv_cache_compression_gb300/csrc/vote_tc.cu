@@ -16,13 +16,16 @@
 //     log2 units; a larger one is reported as SNAPKV_ERR_UNSUPPORTED.
 //   B (vote): once the head's counter shows all its A items, C_j = sum_i 2^(s'_ij - log2 Z_i) for
 //     the item's prefix keys (the softmax max-subtraction cancels between numerator and Z_i).
-// Resident mode (when a head has at most 4 x grid items): the queue holds one item per key chunk;
-// its logits stay in its TMEM slot after the statistics pass, and the warpgroup computes the vote
-// from TMEM once the head is complete, so each key is read by the SM only once. With at most grid
-// items per head a CTA holds at most one item of a head, and the vote follows its own statistics
-// at once; otherwise it follows the statistics of the group's next item, so that a warpgroup never
-// waits while holding an item without pass A: a CTA holds at most four items, two per warpgroup,
-// and at most four items of one head, so the lowest unfinished head always completes.
+// Resident mode (when a head has at most grid items, or, with two epilogue warpgroups or in a ragged
+// batch, at most 4 x grid): the queue holds one item per key chunk; its logits stay in its TMEM slot
+// after the statistics pass, and the warpgroup computes the vote from TMEM once the head is
+// complete, so each key is read by the SM only once. With at most grid items per head a CTA holds
+// at most one item of a head, and the vote follows its own statistics at once (every epilogue
+// warpgroup holds one item, and the MMA fills the free slot ahead); otherwise it follows the
+// statistics of the group's next item, so that a warpgroup never waits while holding an item
+// without pass A: two warpgroups take the items, a CTA holds at most four items, two per
+// warpgroup, and at most four items of one head, so the lowest unfinished head always completes.
+// Longer heads take the re-read mode of items A and B above.
 //
 // A persistent, cooperative grid (one CTA per SM) takes queue positions round-robin. Per CTA:
 //   warp 0      TMA: streams each item's key tiles (128 keys x 128 B per box, 128-byte swizzle)
@@ -32,9 +35,9 @@
 //               tile into the item's TMEM slot (four slots of 128 columns);
 //   warps 2, 3  idle: with warps 0 and 1 they form warpgroup 0, which lowers its registers
 //               (setmaxnreg) so that the epilogue warpgroups can raise theirs;
-//   warps 4..11 epilogue: two warpgroups, one thread per key (TMEM lane); warpgroup g takes the
-//               CTA's items n = g, g + 2, ..., reads their logits with tcgen05.ld and gives the slot
-//               back as soon as it has read it.
+//   warps 4..   epilogue: G warpgroups (three for windows of up to 64 rows, else two), one thread
+//               per key (TMEM lane); warpgroup g takes the CTA's items n = g, g + G, ..., reads
+//               their logits with tcgen05.ld and gives the slot back as soon as it is done with it.
 //
 // Progress: A items never wait, and a B item waits only for A items that come earlier in the queue;
 // every CTA takes its positions in queue order and the cooperative launch keeps all CTAs resident,
@@ -55,19 +58,26 @@ namespace snapkv {
 namespace {
 
 constexpr int kCtlWarps = 4;                       // warpgroup 0: TMA producer, MMA issuer, two idle
-constexpr int kEpiWarps = 8;                       // warpgroups 1 and 2: the epilogue
-constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreadsTc = kCtlWarps * 32 + kEpiThreads;
-// Register split (setmaxnreg): 12 warps put three warps on every SM sub-partition, so the launch
-// gives each thread 168 registers; warpgroup 0 then hands most of its share to the epilogue
-// warpgroups, which hold a 32-row chunk of logits per thread without spilling. The split uses
-// exactly the launch's registers (a larger request would wait for ever), and the host launches
-// the kernel only if the compiler gave it that count.
-constexpr int kLaunchRegs = 168;
-constexpr int kCtlRegs = 56;
-constexpr int kEpiRegs = 224;
-static_assert(kCtlWarps * 32 * kCtlRegs + kEpiThreads * kEpiRegs == kThreadsTc * kLaunchRegs, "register split");
-constexpr int kTeardownBarrier = 3;                // named barrier of all warps before TMEM is freed
+// Epilogue warpgroups and the register split (setmaxnreg) that goes with them. Windows of up to 64
+// rows take three warpgroups: 16 warps give each thread 128 registers at launch, warpgroup 0 lowers
+// itself to 56 and the epilogue raises itself to 136 (a 32-row chunk of logits and the vote's
+// per-row factors of a 64-row window fit). Wider windows keep up to 128 per-row factors in
+// registers and take two warpgroups: 12 warps, 168 registers at launch, 56 and 224. No split asks
+// for more than the launch's registers (a larger request would wait for ever), and the host
+// launches the kernel only if the compiler gave it that count. Fewer groups than TMEM slots is what
+// the queue's progress argument needs (a group holds at most two slots, one with a vote pending).
+template <int N>
+struct EpiCfg {
+  static constexpr int kGroups = N <= 64 ? 3 : 2;
+  static constexpr int kThreads = (kCtlWarps + 4 * kGroups) * 32;
+  static constexpr int kLaunchRegs = kGroups == 3 ? 128 : 168;
+  static constexpr int kCtlRegs = 56;
+  static constexpr int kEpiRegs = kGroups == 3 ? 136 : 224;
+  static_assert(kCtlWarps * 32 * kCtlRegs + kGroups * 128 * kEpiRegs <= kThreads * kLaunchRegs, "register split");
+  static_assert(kCtlRegs % 8 == 0 && kEpiRegs % 8 == 0 && kEpiRegs <= 256, "setmaxnreg counts");
+};
+constexpr int kMaxGroups = 3;
+constexpr int kTeardownBarrier = 1 + kMaxGroups;   // named barrier of all warps before TMEM is freed
 constexpr int kTileKeys = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clock
@@ -172,15 +182,16 @@ struct TcLayout {
   // flight already keep HBM busy, and a deeper ring only lengthens the memory queues that the
   // epilogue's reductions, counter updates and vote stores wait in (8 stages: 39.3 us per launch
   // of the 16K-key layer, 3 stages: 34.6 us).
+  static constexpr int G = EpiCfg<N>::kGroups;
   static constexpr int FIXED =
-      2 * Q_BYTES + 2 * 4 * N * 4 + 2 * N * 4 + kSlots * N * 4 + 8 * (2 * 8 + 4 + 4 * 16 + 4 + 1) + 64 + 1024;
+      2 * Q_BYTES + G * 4 * N * 4 + G * N * 4 + kSlots * N * 4 + 8 * (2 * 8 + 4 + 4 * 16 + 4 + 1) + 64 + 1024;
   static constexpr int STAGES_FIT = (232448 - FIXED) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT < 3 ? STAGES_FIT : 3;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_Q = OFF_K + STAGES * STAGE_BYTES;
-  static constexpr int OFF_RED = OFF_Q + 2 * Q_BYTES;        // [2 groups][4 warps][N] floats
-  static constexpr int OFF_ROW = OFF_RED + 2 * 4 * N * 4;    // [2 groups][N] floats: per-row constants
-  static constexpr int OFF_SMAX = OFF_ROW + 2 * N * 4;      // [kSlots][N] floats: an item's row maxima
+  static constexpr int OFF_RED = OFF_Q + 2 * Q_BYTES;        // [G groups][4 warps][N] floats
+  static constexpr int OFF_ROW = OFF_RED + G * 4 * N * 4;    // [G groups][N] floats: per-row constants
+  static constexpr int OFF_SMAX = OFF_ROW + G * N * 4;      // [kSlots][N] floats: an item's row maxima
   static constexpr int OFF_BAR = OFF_SMAX + kSlots * N * 4;
   static constexpr int NBAR = 2 * STAGES + 4 + kSlots * TI + kSlots + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -230,11 +241,13 @@ __device__ __forceinline__ int tiles_of(const TcArgs& a, const Item& it, int TI)
 }
 
 template <int D, int N, bool VAR>
-__global__ void __launch_bounds__(kThreadsTc, 1)
+__global__ void __launch_bounds__(EpiCfg<N>::kThreads, 1)
 vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                TcParams<VAR> a) {
   using Lay = TcLayout<D, N>;
+  using Epi = EpiCfg<N>;
   constexpr int TI = Lay::TI;
+  constexpr int G = Epi::kGroups;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + Lay::OFF_BAR);
@@ -273,16 +286,16 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
   // within its own register share.
   auto teardown = [&]() {
     __syncwarp();   // the roles' single-lane loops have rejoined their warps
-    ptx::named_barrier(kTeardownBarrier, kThreadsTc);   // every warp is done with TMEM
+    ptx::named_barrier(kTeardownBarrier, Epi::kThreads);   // every warp is done with TMEM
     if (warp == 1) {
       ptx::tc_fence_after();
       ptx::tmem_dealloc(tmem_base, kTmemCols);
     }
   };
   if (warp < kCtlWarps)   // warpgroup-uniform
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Epi::kCtlRegs));
   else
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Epi::kEpiRegs));
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -399,10 +412,10 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     teardown();   // warps 2 and 3 only lend their registers
     return;
   } else {
-    // ------------------------------------------------------------ epilogue (warps 4..11)
+    // ------------------------------------------------------------ epilogue (warps 4 .. 4 + 4G - 1)
     const int q4 = warp & 3;                         // TMEM lane quarter this warp may access
     const int gw = (warp - kCtlWarps) & 3;           // warp within its group
-    const int grp = (warp - kCtlWarps) >> 2;         // group: items n = grp, grp + 2, ...
+    const int grp = (warp - kCtlWarps) >> 2;         // group: items n = grp, grp + ng, ...
     const int gtid = (threadIdx.x - kCtlWarps * 32) & 127;   // thread within its group
     const int bar_id = 1 + grp;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
@@ -410,7 +423,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     constexpr int R = N < 32 ? N : 32;               // rows per register chunk
     float* gred = red + grp * 4 * N;
     float* growc = rowc + grp * N;
-    __shared__ int sh_stop[2];
+    __shared__ int sh_stop[kMaxGroups];
 
     // Abort decision shared by the group's 128 threads (named barriers have no timeout, so every
     // thread of a group must take the same path between them).
@@ -734,11 +747,17 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     };
 
     // With at most grid items per head, the positions of a head's items are less than a grid apart,
-    // so no CTA holds two of them.
+    // so no CTA holds two of them. Otherwise each group holds two items at a time (one waiting for
+    // its vote), and only two groups fit the four TMEM slots: the third one sits out.
     const bool lag0 = a.n_chunk <= (int)gridDim.x;
+    const int ng = (a.resident && !lag0) ? 2 : G;   // groups taking items
+    if (grp >= ng) {
+      teardown();
+      return;
+    }
     int k = 0;
     for (;; ++k) {
-      const int n = grp + 2 * k;
+      const int n = grp + ng * k;
       const int p = blockIdx.x + n * gridDim.x;
       if (p >= a.n_queue || stop_uniform()) break;
       const Item it = queue_item<VAR>(a, p);
@@ -756,12 +775,12 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       } else if (a.resident && k > 0) {
         // Otherwise the vote of the group's previous item, whose logits are still in TMEM, comes
         // after the statistics of this one (so no item of the CTA waits without its pass A).
-        const int m = n - 2;
+        const int m = n - ng;
         item_vote(m, queue_item<VAR>(a, blockIdx.x + m * gridDim.x));
       }
     }
     if (a.resident && !lag0 && k > 0 && !stop_uniform()) {
-      const int m = grp + 2 * (k - 1);
+      const int m = grp + ng * (k - 1);
       item_vote(m, queue_item<VAR>(a, blockIdx.x + m * gridDim.x));
     }
     teardown();
@@ -804,13 +823,20 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   a.keys_per_item = Lay::TI * kTileKeys;
   a.n_chunk = (int)((job.l_prompt + a.keys_per_item - 1) / a.keys_per_item);
   a.bh_total = (int)bh;
-  a.resident = a.n_chunk <= kSlots * grid ? 1 : 0;
+  // Resident mode while a head has at most grid items (the vote follows its own statistics at once)
+  // or, with two epilogue groups, at most four per CTA (the vote comes one item late and each group
+  // holds two TMEM slots). With three groups the late vote would leave one of them idle, and
+  // re-reading the keys from L2 with all three is faster: 384 against 475 us for 32 heads of 131072
+  // keys and a 64-row window.
+  const bool late_fits = a.n_chunk <= kSlots * grid;
+  a.resident = (EpiCfg<N>::kGroups == 3 ? a.n_chunk <= grid : late_fits) ? 1 : 0;
   a.n_queue = (int)((a.resident ? 1 : 2) * bh * a.n_chunk);
   TcParams<true> pv;
   if (job.n_var > 0) {
     // Ragged batch: n_chunk holds the largest head's items (the queue's deadlock-freedom
     // conditions bound the items of a head), and the queue is resident only.
-    if (job.n_var > kMaxVarSeq || group != 1 || !a.resident) return cudaErrorInvalidValue;
+    if (job.n_var > kMaxVarSeq || group != 1 || !late_fits) return cudaErrorInvalidValue;
+    a.resident = 1;
     pv.vs.n = job.n_var;
     pv.vs.heads = job.heads;
     int pos = 0;
@@ -847,7 +873,7 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
   if (grid > a.n_queue) grid = a.n_queue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreadsTc);
+  cfg.blockDim = dim3(EpiCfg<N>::kThreads);
   cfg.dynamicSmemBytes = Lay::BYTES;
   cfg.stream = job.stream;
   cudaLaunchAttribute attr[1];
@@ -889,9 +915,9 @@ cudaError_t launch_tc_typed(const CompressJob& job, int grid) {
 // fewer, the epilogue's request could not be met and its warps would wait for ever): a kernel
 // built with another count is never launched (the grid is reported as not resident).
 template <typename K>
-bool launch_regs_ok(K kernel) {
+bool launch_regs_ok(K kernel, int launch_regs) {
   cudaFuncAttributes fa{};
-  return cudaFuncGetAttributes(&fa, kernel) == cudaSuccess && fa.numRegs == kLaunchRegs;
+  return cudaFuncGetAttributes(&fa, kernel) == cudaSuccess && fa.numRegs == launch_regs;
 }
 
 template <int D, int N>
@@ -910,9 +936,10 @@ int tc_grid() {
           cudaSuccess &&
       cudaFuncSetAttribute(vote_tc_kernel<D, N, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES) ==
           cudaSuccess &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vote_tc_kernel<D, N, false>, kThreadsTc, Lay::BYTES) ==
-          cudaSuccess &&
-      per_sm > 0 && launch_regs_ok(vote_tc_kernel<D, N, false>) && launch_regs_ok(vote_tc_kernel<D, N, true>))
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vote_tc_kernel<D, N, false>, EpiCfg<N>::kThreads,
+                                                    Lay::BYTES) == cudaSuccess &&
+      per_sm > 0 && launch_regs_ok(vote_tc_kernel<D, N, false>, EpiCfg<N>::kLaunchRegs) &&
+      launch_regs_ok(vote_tc_kernel<D, N, true>, EpiCfg<N>::kLaunchRegs))
     grid = sms;
   cache[dev].store(grid, std::memory_order_release);
   return grid > 0 ? grid : 0;

@@ -107,6 +107,24 @@ def test_long_context_every_head(dev):
     print(f"long context: {len(jobs)} heads, {excused} boundary-excused indices")
 
 
+@pytest.mark.parametrize("l_obs,grids,tail", [(100, 2, 333), (100, 4, 777), (64, 1, 999), (32, 4, 777)])
+def test_long_heads_in_every_queue_mode(dev, l_obs, grids, tail):
+    """Heads with more key chunks than the grid has CTAs (one per SM) cannot take the vote right
+    after their own statistics. A window padded to 128 rows (two epilogue warpgroups) keeps the
+    logits in TMEM and votes one item late while a head has at most four chunks per CTA (grids = 2),
+    and past that alternates statistics and vote items that read the keys again from L2 (grids = 4).
+    Windows of up to 64 rows (three warpgroups) take the re-read mode as soon as a head has more
+    chunks than CTAs (grids = 1 and 4). Every prompt ends in a ragged tail."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    n_pad = 128 if l_obs > 64 else (64 if l_obs > 32 else 32)
+    keys_per_item = (128 // n_pad) * 128
+    L = grids * sms * keys_per_item + tail
+    n_chunk = (L + keys_per_item - 1) // keys_per_item
+    assert grids * sms < n_chunk <= grids * sms + 8
+    wl = synth.WORKLOADS[1].with_(heads=2, l_obs=l_obs, l_prompt=L)
+    _run_workload(dev, wl, l_prompt=L, algo="tensor_core")
+
+
 def test_long_context_sampled_heads_simt(dev):
     _run_workload(dev, synth.WORKLOADS[3], heads=[0, 13, 31], algo="simt")
 

@@ -63,6 +63,21 @@ def test_varlen_ratio_rule_bf16(dev, algo):
     _check(res, wl, lengths, range(wl.heads), ratio_p=0.1, budget=0)
 
 
+def test_varlen_longest_prompt_past_one_chunk_per_cta(dev):
+    """A ragged batch keeps every sequence's logits in TMEM; when its longest prompt has more key
+    chunks than the grid has CTAs (one per SM), the vote of an item comes one item late and only two
+    epilogue warpgroups take items. The short sequences share the queue with it."""
+    from kv_cache_compression_gb300 import snapkv
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    wl = synth.WORKLOADS[1].with_(heads=2, plants=16)
+    lengths = [sms * 512 + 2000, 3000, 77]
+    assert (lengths[0] + 511) // 512 > sms   # 512 keys per item for a 32-row window
+    q, k, v = synth.device_inputs_padded(wl, 0, 0, lengths, dev)
+    res = snapkv.compress_varlen(q, k, v, lengths, pool_kernel=wl.pool_kernel, budget=1024, want_vote=True)
+    torch.cuda.synchronize()
+    _check(res, wl, lengths, range(wl.heads), ratio_p=0.0, budget=1024)
+
+
 def test_varlen_tiny_fp32_prefix_only_and_padding_longer_than_any_prompt(dev):
     from kv_cache_compression_gb300 import snapkv
     wl = synth.WORKLOADS[0]

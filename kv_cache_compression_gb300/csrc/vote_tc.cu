@@ -178,15 +178,16 @@ struct TcLayout {
   static constexpr int STAGE_BYTES = KB * A_BYTES;
   static constexpr int QB_BYTES = N * 128;          // one k-block of the window queries
   static constexpr int Q_BYTES = KB * QB_BYTES;
-  // Everything but the key-tile ring, then at most 3 ring stages: 152 SMs x 3 x 32 KB of reads in
-  // flight already keep HBM busy, and a deeper ring only lengthens the memory queues that the
-  // epilogue's reductions, counter updates and vote stores wait in (8 stages: 39.3 us per launch
-  // of the 16K-key layer, 3 stages: 34.6 us).
+  // Everything but the key-tile ring, then at most 4 ring stages: 152 SMs x 4 x 32 KB of reads in
+  // flight keep HBM busy, and a deeper ring only lengthens the memory queues that the epilogue's
+  // reductions, counter updates and vote stores wait in. Measured per launch of the 256-head 16K-key
+  // layer with three epilogue warpgroups: 3 stages 172.7 us, 4 stages 165.2 us, 5 stages 167.7 us
+  // (with two warpgroups on the 32-head layer, 8 stages had measured 39.3 us against 34.6 us).
   static constexpr int G = EpiCfg<N>::kGroups;
   static constexpr int FIXED =
       2 * Q_BYTES + G * 4 * N * 4 + G * N * 4 + kSlots * N * 4 + 8 * (2 * 8 + 4 + 4 * 16 + 4 + 1) + 64 + 1024;
   static constexpr int STAGES_FIT = (232448 - FIXED) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT < 3 ? STAGES_FIT : 3;
+  static constexpr int STAGES = STAGES_FIT < 4 ? STAGES_FIT : 4;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_Q = OFF_K + STAGES * STAGE_BYTES;
   static constexpr int OFF_RED = OFF_Q + 2 * Q_BYTES;        // [G groups][4 warps][N] floats

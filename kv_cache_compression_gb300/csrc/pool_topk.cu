@@ -430,10 +430,22 @@ pool_topk_cluster_kernel(const float* __restrict__ c_all, int32_t* __restrict__ 
     uint32_t* s = sums + (pass & 1) * kMaxBins;
     for (int b = tid; b < nb; b += kCThreads) hist[b] = 0u;
     __syncthreads();
-    for (int jb = 0; jb < n; jb += kCThreads) {   // warp-uniform trip count
-      const int j = jb + tid;
-      const uint32_t u = j < n ? pbits[j] : 0u;
-      warp_hist_add(hist, (u >> shift) & (uint32_t)(nb - 1), j < n && (u & mask) == prefix);
+    if (pass == 0) {
+      // Every value counts, and a warp's 32 neighbouring values mostly share their top digit: the
+      // warp adds each distinct digit once.
+      for (int jb = 0; jb < n; jb += kCThreads) {   // warp-uniform trip count
+        const int j = jb + tid;
+        const uint32_t u = j < n ? pbits[j] : 0u;
+        warp_hist_add(hist, (u >> shift) & (uint32_t)(nb - 1), j < n);
+      }
+    } else {
+      // Only the values in the chosen bin count (a few percent), spread over the lower digits:
+      // plain shared-memory atomics (256-head layer: 62.4 -> 60.4 us per launch against the
+      // warp-aggregated add).
+      for (int j = tid; j < n; j += kCThreads) {
+        const uint32_t u = pbits[j];
+        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & (uint32_t)(nb - 1)], 1u);
+      }
     }
     __syncthreads();
     const uint32_t* whole = hist;   // the head's histogram

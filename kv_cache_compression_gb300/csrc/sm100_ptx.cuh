@@ -78,7 +78,6 @@ __device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const CUtensorM
       : "memory");
 }
 
-// Prefetch one tensor tile into L2 (no shared memory, no completion tracking).
 // Contiguous copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from global memory
 // into this CTA's shared memory, completing on `bar` (complete_tx).
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
@@ -146,7 +145,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 32 lanes x 32 bit, 16 / 32 consecutive columns per thread.
 // Stores 16 consecutive 32-bit columns of this thread's TMEM lane (the layout tmem_ld16 reads).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
   asm volatile(
@@ -158,6 +156,8 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
       : "memory");
 }
 
+// Loads 16 consecutive 32-bit columns of this thread's TMEM lane (32 lanes x 32 bit: each warp reads
+// its own quarter of the 128 lanes).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
   asm volatile(
@@ -167,11 +167,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
       : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  tmem_ld16(taddr, v);
-  tmem_ld16(taddr + 16, v + 16);
 }
 
 // Shared-memory matrix descriptor of a K-major bf16 tile stored as rows of 128 bytes with the
@@ -252,13 +247,6 @@ __device__ __forceinline__ void dsmem_add_u32(uint32_t addr, uint32_t v) {
 
 __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// 16-byte load from another CTA's shared memory (ordered by the surrounding cluster barriers).
-__device__ __forceinline__ uint4 dsmem_ld_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
 }
 
 __device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr) {

@@ -64,10 +64,11 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the measurements after the timed region (single layer, full-cache decode, hit "
                          "rate, GQA, varlen, long context); used for profiler captures of the step alone")
-    ap.add_argument("--case", choices=["prefill-layer", "decode-layer"], default=None,
+    ap.add_argument("--case", choices=["prefill-layer", "decode-layer", "llama-layer"], default=None,
                     help="a small profiling case instead of the benchmark: one layer of the headline prefill "
-                         "(2 GiB of K/V) compressed --steps times, or one layer of the decode workload's cache "
-                         "(2.3 GB) decoded --steps times")
+                         "(2 GiB of K/V) compressed --steps times, one layer of the decode workload's cache "
+                         "(2.3 GB) decoded --steps times, or the single B1 Llama-2-7B-shaped layer (4 input "
+                         "copies, 1 GiB of K/V) compressed and decoded one step --steps times")
     return ap.parse_args()
 
 
@@ -870,10 +871,9 @@ def decode_leg(torch, snapkv, synth, dev, world, rank=0, passes=2, sample_clocks
 # Single-layer workload (extra): one Llama-2-7B-shaped layer, B1, budget 1024, planted keys
 # ------------------------------------------------------------------------------------------------
 
-def single_layer_extra(torch, snapkv, synth, dev, n_steps=200, copies=4):
-    """One layer (B1 H32 d128 bf16, L_prompt 16384, L_obs 32, K_pool 7, budget 1024, 64 planted keys per
-    head) + one decode step, as CUDA graph replays over 4 input copies (1 GiB of K/V > L2), with the
-    score/vote kernel's own time from event nodes."""
+def setup_single_layer(torch, snapkv, synth, dev, copies=4):
+    """The Llama-2-7B-shaped layer (B1 H32 d128 bf16, L_prompt 16384, L_obs 32, K_pool 7, budget 1024, 64
+    planted keys per head) in `copies` input copies, with its compressed caches and workspaces."""
     wl = synth.WORKLOADS[1]
     B, H, d, L, lo = 1, wl.heads, wl.head_dim, wl.l_prompt, wl.l_obs
     params = snapkv.make_params(batch=B, heads=H, head_dim=d, l_obs=lo, l_prompt=L, pool_kernel=wl.pool_kernel,
@@ -897,6 +897,13 @@ def single_layer_extra(torch, snapkv, synth, dev, n_steps=200, copies=4):
                         layers=layers, status=torch.zeros((1,), dtype=torch.int32, device=dev),
                         ws_c=snapkv.new_workspace(snapkv.compress_workspace_size(params), dev),
                         ws_d=snapkv.new_workspace(snapkv.decode_workspace_size(B, H, d, cap), dev))
+    return m
+
+
+def single_layer_extra(torch, snapkv, synth, dev, n_steps=200, copies=4):
+    """One layer (setup_single_layer) + one decode step, as CUDA graph replays over 4 input copies (1 GiB
+    of K/V > L2), with the score/vote kernel's own time from event nodes."""
+    m = setup_single_layer(torch, snapkv, synth, dev, copies)
     stream = torch.cuda.current_stream(dev)
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
@@ -959,6 +966,13 @@ def run_case(args, local_rank):
             launch_layer(m, snapkv, 0, stream)
         torch.cuda.synchronize(dev)
         check_status(m, snapkv, "prefill-layer case")
+        print(json.dumps({"case": args.case, "calls": args.steps, "kept": m.ksel, "heads": m.B * m.H}))
+    elif args.case == "llama-layer":
+        m = setup_single_layer(torch, snapkv, synth, dev)
+        for i in range(max(1, args.steps)):
+            launch_layer(m, snapkv, i % m.n_layers, stream)
+        torch.cuda.synchronize(dev)
+        check_status(m, snapkv, "llama-layer case")
         print(json.dumps({"case": args.case, "calls": args.steps, "kept": m.ksel, "heads": m.B * m.H}))
     else:
         m = setup_decode(torch, snapkv, synth, dev, layers=1)

@@ -13,6 +13,7 @@ import torch
 import synth
 from oracle import snapkv_oracle as orc
 from tests import oracle_pool
+from tests.conftest import golden
 from tests.parity import assert_canary, bf16_bits, canary_like, check_compress_head, to_numpy_f32
 
 pytestmark = pytest.mark.gpu
@@ -123,6 +124,20 @@ def test_long_heads_in_every_queue_mode(dev, l_obs, grids, tail):
     assert grids * sms < n_chunk <= grids * sms + 8
     wl = synth.WORKLOADS[1].with_(heads=2, l_obs=l_obs, l_prompt=L)
     _run_workload(dev, wl, l_prompt=L, algo="tensor_core")
+
+
+_PRESETS = [(pre["name"], pre["l_obs"], pre["pool_kernel"], budget)
+            for pre in golden("snapkv_presets.json")["presets"] for budget in sorted(set(pre["max_kept"]))]
+
+
+@pytest.mark.parametrize("name,l_obs,pool,budget", _PRESETS, ids=lambda x: str(x))
+def test_explainer_presets_on_the_tensor_core_path(dev, name, l_obs, pool, budget):
+    """The hyper-parameter presets of the explainer's implementation section (observation window,
+    pooling kernel, kept budget) on the default tensor-core path, every head of B2 H4 with a
+    9000-key prompt (a ragged last tile): windows of 16, 32 and 64 rows, kernels of 5, 7 and 13."""
+    wl = synth.WORKLOADS[1].with_(batch=2, heads=4, l_obs=l_obs, pool_kernel=pool, budget=budget, l_prompt=9000,
+                                  plants=16)
+    _run_workload(dev, wl, l_prompt=9000, algo="tensor_core")
 
 
 def test_long_context_sampled_heads_simt(dev):

@@ -66,6 +66,41 @@ def test_fuzz_compress(dev, case):
                                     l_prefix=l_prefix, l_obs=l_obs, where=f"fuzz {i} {algo} b{b} h{h}")
 
 
+def _long_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        l_obs = int(rng.choice([5, 16, 24, 32, 40, 64, 65, 100]))
+        L = int(rng.integers(20000, 90000))
+        pool = int(rng.choice([1, 5, 7, 13, 31]))
+        if rng.integers(0, 2):
+            p, budget = float(rng.choice([0.01, 0.05, 0.2])), 0
+        else:
+            p, budget = 0.0, int(rng.integers(1, 8192))
+        cases.append((i, l_obs, L, pool, p, budget))
+    return cases
+
+
+@pytest.mark.parametrize("case", _long_cases(8, 777001), ids=lambda c: f"long{c[0]}")
+def test_fuzz_long_prompts(dev, case):
+    """Long random prompts on the default path, so that heads of more items than the grid has CTAs
+    take the vote kernel's late-vote or key re-read modes, and prefixes beyond one CTA take clusters in
+    the top-k kernel."""
+    from kv_cache_compression_gb300 import snapkv
+    i, l_obs, L, pool, p, budget = case
+    wl = synth.Workload(f"long fuzz {i}", 900 + i, bf16=True, batch=1, heads=2, head_dim=128, layers=1,
+                        l_prompt=L, l_obs=l_obs, pool_kernel=pool, ratio_p=p, budget=budget)
+    q, k, v, _ = synth.device_inputs(wl, 0, 0, 1, L, dev)
+    res = snapkv.compress(q, k, v, pool_kernel=pool, ratio_p=p, budget=budget, want_vote=True)
+    torch.cuda.synchronize()
+    for h in range(2):
+        hi = synth.host_head(wl, 0, 0, h, l_prompt=L)
+        ref = orc.compress_head(hi.q_obs, hi.k, hi.v, pool_kernel=pool, ratio_p=p, budget=budget)
+        check_compress_head(gpu_idx=res["idx"][0, h].cpu().numpy()[:res["k"]], gpu_kc=to_numpy_f32(res["k_out"][0, h]),
+                            gpu_vc=to_numpy_f32(res["v_out"][0, h]), gpu_vote=res["vote"][0, h].cpu().numpy(),
+                            ref=ref, k_in=hi.k, v_in=hi.v, l_prefix=L - l_obs, l_obs=l_obs, where=f"long fuzz {i} h{h}")
+
+
 @pytest.mark.parametrize("seed", [1, 2, 3, 8, 9])
 def test_fuzz_varlen(dev, seed):
     from kv_cache_compression_gb300 import snapkv

@@ -15,6 +15,7 @@ cache per layer (74 GB over the 32 layers), then 128 decode steps x 32 layers of
 snapkv_append_decode_attend, timed as a whole (one CUDA graph of 4096 launches).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --case prefill-layer|decode-layer|llama-layer [--steps K]   # small cases for ncu
 
 --impl reference times the CPU oracle (float64 numpy, one head per step on one core) on the headline
 workload. Under torchrun every rank runs its own replica (independent sequences: weak scaling, no

@@ -933,10 +933,11 @@ def single_layer_extra(torch, snapkv, synth, dev, n_steps=200, copies=4):
                                64, dev, copies)
     check_status(m, snapkv, "single layer")
     mean = {s: statistics.fmean(v) for s, v in samples.items()}
+    wl, ksel, H, L = m.wl, m.ksel, m.H, m.L
     alg = algorithmic_bytes(wl, ksel)
     peak, _ = read_peaks()
     vote_gbs = alg["score+vote"] * H / (mean["score"] * 1e-3) / 1e9
-    del m, graphs, layers
+    del m, graphs
     torch.cuda.empty_cache()
     return {"workload": "Llama-2-7B-shaped layer: B1 H32 d128 bf16, L_prompt 16384, L_obs 32, K_pool 7, budget "
                         "1024 (64 planted keys/head), + 1 decode step",

@@ -468,10 +468,10 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     auto item_stats = [&](int n, const Item& it) {
       const int slot = n % kSlots;
       const int tiles = tiles_of<VAR>(a, it, TI);
-      const int64_t item_key0 = (int64_t)it.chunk * a.keys_per_item;
-      const int64_t l_prompt = prompt_of<VAR>(a, it);
-      const int64_t l_prefix = VAR ? l_prompt - a.l_obs : a.l_prefix;
-      const int64_t lim = a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? l_prefix : l_prefix - 1;
+      const int item_key0 = it.chunk * a.keys_per_item;
+      const int l_prompt = (int)prompt_of<VAR>(a, it);
+      const int l_prefix = VAR ? l_prompt - a.l_obs : (int)a.l_prefix;
+      const int lim = a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? l_prefix : l_prefix - 1;
       wait_tiles(slot, n / kSlots);
 #pragma unroll 1
       for (int r0 = 0; r0 < N; r0 += R) {
@@ -481,12 +481,12 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         for (int t = 0; t < tiles; ++t) {
           float acc[R];
           load_rows((uint32_t)(slot * TI * N + t * N + r0), acc);
-          const int64_t tkey0 = item_key0 + t * kTileKeys;
+          const int tkey0 = item_key0 + t * kTileKeys;
           if (tkey0 + kTileKeys <= l_prefix) {
 #pragma unroll
             for (int i = 0; i < R; ++i) v[i] = fmaxf(v[i], acc[i]);
           } else {
-            const int64_t key = tkey0 + key_in_tile;
+            const int key = tkey0 + key_in_tile;
 #pragma unroll
             for (int i = 0; i < R; ++i) {
               const int row = r0 + i;
@@ -516,7 +516,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
           float acc[R];
           const uint32_t col = (uint32_t)(slot * TI * N + t * N + r0);
           load_rows(col, acc);
-          const int64_t tkey0 = item_key0 + t * kTileKeys;
+          const int tkey0 = item_key0 + t * kTileKeys;
           if (tkey0 + kTileKeys <= l_prefix) {
 #pragma unroll
             for (int i = 0; i < R; ++i) {
@@ -524,7 +524,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
               v[i] += acc[i];
             }
           } else {
-            const int64_t key = tkey0 + key_in_tile;
+            const int key = tkey0 + key_in_tile;
 #pragma unroll
             for (int i = 0; i < R; ++i) {
               const int row = r0 + i;
@@ -573,10 +573,10 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     auto item_stats_pairs = [&](int n, const Item& it) {
       const int slot = n % kSlots;
       const int tiles = tiles_of<VAR>(a, it, TI);
-      const int64_t item_key0 = (int64_t)it.chunk * a.keys_per_item;
-      const int64_t l_prompt = prompt_of<VAR>(a, it);
-      const int64_t l_prefix = VAR ? l_prompt - a.l_obs : a.l_prefix;
-      const int64_t lim = a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? l_prefix : l_prefix - 1;
+      const int item_key0 = it.chunk * a.keys_per_item;
+      const int l_prompt = (int)prompt_of<VAR>(a, it);
+      const int l_prefix = VAR ? l_prompt - a.l_obs : (int)a.l_prefix;
+      const int lim = a.scope == SNAPKV_SCOPE_PROMPT_CAUSAL ? l_prefix : l_prefix - 1;
       // Folds the visible logits of rows rb .. rb + R - 1 of tile t into v (max, or sum of 2^(s'-M));
       // the sum also writes each 2^(s'-M) (0 where not visible) back over its logit for the vote of
       // a resident item.
@@ -584,7 +584,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         float acc[R];
         const uint32_t col = (uint32_t)(slot * TI * N + t * N + rb);
         load_rows(col, acc);
-        const int64_t tkey0 = item_key0 + t * kTileKeys;
+        const int tkey0 = item_key0 + t * kTileKeys;
         if (tkey0 + kTileKeys <= l_prefix) {
 #pragma unroll
           for (int i = 0; i < R; ++i) {
@@ -596,7 +596,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
             }
           }
         } else {
-          const int64_t key = tkey0 + key_in_tile;
+          const int key = tkey0 + key_in_tile;
 #pragma unroll
           for (int i = 0; i < R; ++i) {
             const int row = rb + i;
@@ -677,7 +677,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     auto item_vote = [&](int n, const Item& it) {
       const int slot = n % kSlots;
       const int tiles = tiles_of<VAR>(a, it, TI);
-      const int64_t item_key0 = (int64_t)it.chunk * a.keys_per_item;
+      const int item_key0 = it.chunk * a.keys_per_item;
       if (gtid == 0) {
         const uint32_t need =
             VAR ? (uint32_t)((it.l_prompt + a.keys_per_item - 1) / a.keys_per_item) : (uint32_t)a.n_chunk;
@@ -712,10 +712,10 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       float cr[N];
 #pragma unroll
       for (int i = 0; i < N; ++i) cr[i] = growc[i];
-      const int64_t vote_end = VAR ? prompt_of<VAR>(a, it) - a.l_obs : a.l_prefix;   // prefix keys only
+      const int vote_end = VAR ? (int)prompt_of<VAR>(a, it) - a.l_obs : (int)a.l_prefix;   // prefix keys only
       if (a.resident) {
         for (int t = 0; t < tiles; ++t) {
-          const int64_t key = item_key0 + t * kTileKeys + key_in_tile;
+          const int key = item_key0 + t * kTileKeys + key_in_tile;
           float csum = 0.f;
 #pragma unroll
           for (int r0 = 0; r0 < N; r0 += R) {
@@ -729,7 +729,7 @@ vote_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         }
       } else {
         for (int t = 0; t < tiles; ++t) {
-          const int64_t key = item_key0 + t * kTileKeys + key_in_tile;
+          const int key = item_key0 + t * kTileKeys + key_in_tile;
           float csum = 0.f;
 #pragma unroll
           for (int r0 = 0; r0 < N; r0 += R) {
